@@ -1,0 +1,71 @@
+"""The CPU oracle against its pins, and planted mistakes that the pins catch.
+
+No GPU.  Each planted mistake is a textual change to a private copy of
+oracle/gemm_oracle.c (the oracle itself is never modified): a dropped term, a
+transposed operand, wrong signs, an off-by-one exponent bias, a broken
+subnormal scale, ties rounded away from even, a wrong row stride, a missing
+absolute value, a wrong sampled index.  Every one must fail at least one pin.
+"""
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+
+@pytest.fixture(scope="module")
+def real_oracle():
+    return oracle.default()
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(real_oracle, pin):
+    pin(real_oracle)
+
+
+# (description, text in gemm_oracle.c, replacement)
+MUTANTS = [
+    ("drops the last k term", "for (int64_t k = 0; k < K; ++k) {\n                const double p = ai[k] * bj[k];",
+     "for (int64_t k = 0; k + 1 < K; ++k) {\n                const double p = ai[k] * bj[k];"),
+    ("reads B as K×N instead of N×K", "const double p = ai[k] * bj[k];",
+     "const double p = ai[k] * b[k * N + j];"),
+    ("negates the first product", "                acc += p;\n                mag += fabs(p);\n            }\n            C[i * N + j]",
+     "                acc += (k == 0 ? -p : p);\n                mag += fabs(p);\n            }\n            C[i * N + j]"),
+    ("exponent bias off by one", "const int bias = (1 << (eb - 1)) - 1;\n    const int sign",
+     "const int bias = (1 << (eb - 1));\n    const int sign"),
+    ("subnormal scale off by one", "v = ldexp((double)f, 1 - bias - fb);",
+     "v = ldexp((double)f, -bias - fb);"),
+    ("rounds ties away from zero", "if (rem > 0.5 || (rem == 0.5 && (n & 1))) n += 1;",
+     "if (rem >= 0.5) n += 1;"),
+    ("wrong row stride of A", "const double* ai = a + i * K;", "const double* ai = a + i;"),
+    ("magnitude sum without abs", "                mag += fabs(p);\n            }\n            C[i * N + j]",
+     "                mag += p;\n            }\n            C[i * N + j]"),
+    ("sampled entries swap row and column", "const uint16_t* ai = A + I[t] * K;\n        const uint16_t* bj = B + J[t] * K;",
+     "const uint16_t* ai = A + (J[t] < M ? J[t] : I[t]) * K;\n        const uint16_t* bj = B + (I[t] < N ? I[t] : J[t]) * K;"),
+    ("overflow saturates instead of going to infinity",
+     "if (e_field >= emax_field) return sign | (uint16_t)((uint32_t)emax_field << fb);  /* overflow */",
+     "if (e_field >= emax_field) return sign | (uint16_t)(((uint32_t)(emax_field - 1) << fb) | ((1u << fb) - 1));"),
+]
+
+
+@pytest.mark.parametrize("desc,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, desc, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/found: {desc}"
+    mutated = tmp_path / "gemm_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
+    mutant = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(mutant)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except Exception as e:  # a crash in a mutant also counts as caught
+            failed.append(f"{pin.__name__}:{type(e).__name__}")
+    assert failed, f"no pin caught the planted mistake: {desc}"
