@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 dense GEMM C = A·Bᵀ (TFLOP/s) and its roofline fraction.
+
+One step = one C = A·Bᵀ over the whole workload (one launch of the persistent
+kernel).  Default workload: bf16 M=N=K=4096, bf16 out, A and B ~ N(0,1),
+seed 1 (the shape the Mojo Blackwell series is measured on).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: K steps, each bracketed by CUDA events on the launching stream, with
+L2 flushed (a 512 MiB device write) before every step, outside the events.
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the product shards into independent problems; there
+is no data-path collective); value = all ranks' FLOPs ÷ the slowest rank's
+time.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (fp64 triple loop, test
+infrastructure) on the host cores, each step a bounded row-block sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+PAGES_B200_TFLOPS = 293.6   # bf16 4096^3, Mojo part-2 kernel 4 on B200 (context, another machine)
+METRIC = "GEMM TFLOP/s on 1 GB300 (bf16 4096³) and % of dense tensor-core roofline"
+KERNEL_NAME = "gemm_tn_persistent"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="gemm_4096_bf16", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--cta-pair", type=int, default=0, help="force 1 or 2 (0 = library default)")
+    ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (its digest line must match); else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{KERNEL_NAME}_{workload}.txt")
+    try:
+        fields = dict(line.split(":", 1) for line in open(path) if ":" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    if fields.get("source_digest", "").strip() != source_digest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def cpu_baseline(w: wl.Workload, A_bits, B_bits, budget_s: float):
+    """The oracle as it stands on a row-block sample of the workload."""
+    import oracle
+    o = oracle.default()
+    r0 = min(w.M, 8)
+    t0 = time.perf_counter()
+    o.gemm(A_bits[:r0], B_bits, w.dtype)
+    dt0 = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, r0 * budget_s / max(dt0, 1e-6))))
+    t0 = time.perf_counter()
+    o.gemm(A_bits[:rows], B_bits, w.dtype)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of A against all of B ({rows}x{w.N}x{w.K}), {dt:.1f} s, "
+                      f"fp64 triple loop incl. operand decode"}
+
+
+def run_reference(args, w: wl.Workload):
+    rank, _, world = dist_info()
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    o = oracle.default()
+    A, B = wl.make_inputs(w)
+    A_bits, B_bits = wl.as_bits(A), wl.as_bits(B)
+    total_budget = 150.0
+    per_step = min(30.0, total_budget / max(1, args.steps + args.warmup))
+    t0 = time.perf_counter()
+    o.gemm(A_bits[:1], B_bits, w.dtype)
+    one = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, per_step / max(one, 1e-6))))
+    for _ in range(args.warmup):
+        o.gemm(A_bits[:rows], B_bits, w.dtype)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        o.gemm(A_bits[:rows], B_bits, w.dtype)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = 2.0 * rows * w.N * w.K / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": wl.DTYPE_NAMES[w.dtype],
+                   "out": wl.DTYPE_NAMES[w.out_dtype], "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"each step: rows 0..{rows - 1} of A against all of B "
+                                   f"({rows}x{w.N}x{w.K}), fp64 triple loop incl. operand decode"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    rank, local, world = dist_info()
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    import dense_gemm_blackwell_persistent_gb300 as g
+
+    plan = g.gemm_plan_create(local)
+    if args.cta_pair:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, args.cta_pair)
+    if args.group_m:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_GROUP_M, args.group_m)
+
+    A_cpu, B_cpu = wl.make_inputs(w)
+    A, B = A_cpu.cuda(), B_cpu.cuda()
+    out_t = wl.TORCH_DTYPES[w.out_dtype]
+    C = torch.empty((w.M, w.N), dtype=out_t, device="cuda")
+    flush = None if args.no_flush else torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step():
+        g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype, sp)
+
+    for _ in range(max(3, args.warmup)):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if g.gemm_plan_status(plan) != 0:
+        raise SystemExit("device status error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    status = g.gemm_plan_status(plan)
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms_total = sum(launch_ms)
+    if world > 1:
+        t = torch.tensor([kernel_ms_total], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        kernel_ms_total = float(t.item())
+    ms_per_step = kernel_ms_total / args.steps
+    value = world * w.flops * args.steps / (kernel_ms_total / 1e3) / 1e12
+    avg_launch_ms = statistics.mean(launch_ms)
+    achieved = w.flops / (avg_launch_ms / 1e3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    traffic = recorded_traffic(w.name)
+
+    extra = {}
+    if not args.no_cublas and rank == 0 and w.out_dtype == w.dtype:
+        Bt = B.t()
+        for _ in range(5):
+            torch.matmul(A, Bt)
+        cs, ce = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cms = []
+        for _ in range(50):
+            if flush is not None:
+                flush.zero_()
+            cs.record(stream)
+            torch.matmul(A, Bt)
+            ce.record(stream)
+            ce.synchronize()
+            cms.append(cs.elapsed_time(ce))
+        cm = statistics.mean(cms)
+        extra["cublas_reference"] = {"value": w.flops / (cm / 1e3) / 1e12, "unit": "TFLOP/s",
+                                     "ms": cm, "how": "torch.matmul(A, B.t()) same inputs, same process, 50 runs"}
+
+    e2e = None
+    if not args.no_e2e:
+        Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
+        Ch = torch.empty((w.M, w.N), dtype=out_t).pin_memory()
+        g.gemm_plan_run_host(plan, Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), w.M, w.N, w.K, w.dtype,
+                             w.out_dtype, sp)
+        es = []
+        for _ in range(args.e2e_steps):
+            t0 = time.perf_counter()
+            g.gemm_plan_run_host(plan, Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), w.M, w.N, w.K, w.dtype,
+                                 w.out_dtype, sp)
+            es.append(time.perf_counter() - t0)
+        e2e_s = statistics.mean(es)
+        e2e_total = e2e_s * args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_total], dtype=torch.float64, device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_total = float(t.item())
+        e2e = {"value": world * w.flops * args.e2e_steps / e2e_total / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (w.M + w.N) * w.K * wl.ELEM_BYTES[w.dtype],
+               "d2h_bytes_per_step": w.M * w.N * wl.ELEM_BYTES[w.out_dtype],
+               "how": "gemm_plan_run_host: pinned host A,B in, host C out, copies + kernel + sync per step, "
+                      f"host wall clock, {args.e2e_steps} steps"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, wl.as_bits(A_cpu), wl.as_bits(B_cpu), args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / PAGES_B200_TFLOPS if w.name == "gemm_4096_bf16" else None,
+            "dtype": wl.DTYPE_NAMES[w.dtype], "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": wl.DTYPE_NAMES[w.dtype],
+                       "out": wl.DTYPE_NAMES[w.out_dtype], "accumulate": "f32",
+                       "inputs": w.describe(), "parallelism": f"replicas x{world}",
+                       "l2": "not flushed" if args.no_flush else "flushed before every step (512 MiB write)",
+                       "cta_pair": args.cta_pair or 2, "grid_ctas": g.gemm_plan_last_grid(plan),
+                       "vs_baseline_ref": "pages' 293.6 TFLOP/s, Mojo part-2 kernel 4 on B200 (context)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src}: MEASURED_PEAKS bf16_tflops (burst, cuBLAS 8192^3)"},
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "timed_wall_s": wall,
+            "launch_ms": {"mean": avg_launch_ms, "min": min(launch_ms), "median": statistics.median(launch_ms)},
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    g.gemm_plan_destroy(plan)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+"""Python binding of the GB300 dense GEMM library (C = A·Bᵀ).
+
+Argument marshalling only: every function forwards to the extern "C" entry
+point of the same name in ``_lib/libgb300gemm.so`` (declared in
+include/gemm.h).  All arithmetic runs in the library's CUDA kernels.  If the
+compiled library is missing, importing this package raises at once: there is
+no fallback implementation.
+
+``matmul`` is a convenience for torch tensors: it checks shapes, allocates C
+with torch (memory only) and calls ``gemm_plan_run`` on the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+GEMM_BF16, GEMM_F16, GEMM_F32 = 0, 1, 2
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_UNSUPPORTED = -2
+GEMM_ERR_MISALIGNED = -3
+GEMM_ERR_CUDA = -4
+GEMM_ERR_DRIVER = -5
+GEMM_ERR_NO_PLAN = -6
+GEMM_ERR_TIMEOUT = -7
+GEMM_ERR_NO_DEVICE = -8
+GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS = 1, 2, 3
+
+LIB_PATH = _build.LIB
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -m dense_gemm_blackwell_persistent_gb300._build, or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+_lib.gemm_plan_create.argtypes = [ctypes.POINTER(_vp), _int, ctypes.c_uint]
+_lib.gemm_plan_set_option.argtypes = [_vp, _int, _i64]
+_lib.gemm_run.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.gemm_plan_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.gemm_plan_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.gemm_plan_destroy.argtypes = [_vp]
+_lib.gemm_strerror.argtypes = [_int]
+_lib.gemm_strerror.restype = ctypes.c_char_p
+for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_plan_run",
+              "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_destroy"):
+    getattr(_lib, _name).restype = _int
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gemm_strerror(status)} ({status})")
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != GEMM_OK:
+        raise GemmError(rc, where)
+    return rc
+
+
+def gemm_strerror(status: int) -> str:
+    return _lib.gemm_strerror(int(status)).decode()
+
+
+def gemm_plan_create(device: int = -1, flags: int = 0) -> int:
+    h = _vp()
+    _check(_lib.gemm_plan_create(ctypes.byref(h), int(device), int(flags)), "gemm_plan_create")
+    return h.value
+
+
+def gemm_plan_set_option(plan: int, option: int, value: int) -> None:
+    _check(_lib.gemm_plan_set_option(_vp(plan), int(option), int(value)), "gemm_plan_set_option")
+
+
+def gemm_run(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int, out_dtype: int,
+             stream: int = 0) -> None:
+    _check(_lib.gemm_run(_vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, _vp(stream)), "gemm_run")
+
+
+def gemm_plan_run(plan: int, A: int, B: int, C: int, M: int, N: int, K: int, dtype: int,
+                  out_dtype: int, stream: int = 0) -> None:
+    _check(_lib.gemm_plan_run(_vp(plan), _vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype,
+                              _vp(stream)), "gemm_plan_run")
+
+
+def gemm_plan_run_host(plan: int, A_host: int, B_host: int, C_host: int, M: int, N: int, K: int,
+                       dtype: int, out_dtype: int, stream: int = 0) -> None:
+    _check(_lib.gemm_plan_run_host(_vp(plan), _vp(A_host), _vp(B_host), _vp(C_host), M, N, K,
+                                   dtype, out_dtype, _vp(stream)), "gemm_plan_run_host")
+
+
+def gemm_plan_status(plan: int) -> int:
+    st = _int(0)
+    _check(_lib.gemm_plan_status(_vp(plan), ctypes.byref(st)), "gemm_plan_status")
+    return st.value
+
+
+def gemm_plan_last_grid(plan: int) -> int:
+    n = _int(0)
+    _check(_lib.gemm_plan_last_grid(_vp(plan), ctypes.byref(n)), "gemm_plan_last_grid")
+    return n.value
+
+
+def gemm_plan_destroy(plan: int) -> None:
+    _check(_lib.gemm_plan_destroy(_vp(plan)), "gemm_plan_destroy")
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Call a C entry point with raw ctypes arguments and return its status code
+    (used by tests that check error returns)."""
+    return int(getattr(_lib, fn_name)(*args))
+
+
+# ------------------------------------------------------------------ torch helpers
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.bfloat16: GEMM_BF16, torch.float16: GEMM_F16, torch.float32: GEMM_F32}
+    if t not in codes:
+        raise TypeError(f"unsupported dtype {t}")
+    return codes[t]
+
+
+def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None):
+    """C = A @ B.T for CUDA tensors A [M,K], B [N,K] (bf16 or f16, contiguous).
+
+    out_dtype: torch.float32, torch.bfloat16 or torch.float16 (default: A's dtype).
+    Runs on torch's current stream of A's device.
+    """
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be [M,K] and B [N,K]")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous row-major")
+    out_dtype = A.dtype if out_dtype is None else out_dtype
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M,N] tensor of out_dtype")
+    stream = torch.cuda.current_stream(A.device).cuda_stream
+    args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, _dtype_code(A.dtype),
+            _dtype_code(out_dtype), stream)
+    if plan is None:
+        gemm_run(*args)
+    else:
+        gemm_plan_run(plan, *args)
+    return out

@@ -1,0 +1,414 @@
+// gemm_api.cu -- host side of the library: argument checks, tensor-map
+// construction, plan registry, launch of the persistent kernel, and the
+// extern "C" entry points declared in include/gemm.h.
+//
+// The tensor map is the host-built descriptor of "Optimizing Blackwell
+// Matrix Multiplication in Mojo (Part 2)", "Loading tiles into shared
+// memory" (shape, strides, global address, box size and swizzle mode in one
+// opaque block handed to the kernel).  It is encoded with the driver's
+// cuTensorMapEncodeTiled, fetched at run time through the runtime's
+// driver-entry-point query so the library does not link libcuda directly.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using namespace gb300;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+std::vector<gemm_plan*> g_plans[kMaxDevices];  // live plans per device, newest last
+EncodeTiledFn g_encode = nullptr;
+
+int elem_bytes(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+
+CUtensorMapDataType tma_dtype(int dt) {
+    switch (dt) {
+        case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+int get_encoder(EncodeTiledFn* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_DRIVER;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = g_encode;
+    return GEMM_OK;
+}
+
+// Row-major matrix rows×cols (cols contiguous), box = box_rows × box_cols,
+// 128-byte swizzle, zero fill outside the matrix.
+int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint32_t box_cols, CUtensorMapL2promotion promo) {
+    EncodeTiledFn enc;
+    int rc = get_encoder(&enc);
+    if (rc != GEMM_OK) return rc;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes(dt)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, tma_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
+
+template <int kPair>
+KernelFn kernel_for(int out) {
+    switch (out) {
+        case GEMM_BF16: return gemm_tn_persistent<kPair, kOutBF16>;
+        case GEMM_F16: return gemm_tn_persistent<kPair, kOutF16>;
+        default: return gemm_tn_persistent<kPair, kOutF32>;
+    }
+}
+
+KernelFn pick_kernel(int pair, int out) { return pair == 2 ? kernel_for<2>(out) : kernel_for<1>(out); }
+int smem_bytes(int pair) { return pair == 2 ? Cfg<2>::kSmemBytes : Cfg<1>::kSmemBytes; }
+
+uint32_t make_idesc(int in_dtype, int m, int n) {
+    const uint32_t ab = in_dtype == GEMM_BF16 ? 1u : 0u;  // operand format: 0 = f16, 1 = bf16
+    return (1u << 4)                   // accumulator format: f32
+           | (ab << 7) | (ab << 10)    // A and B formats
+           | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);  // both K-major (bits 15/16 = 0)
+}
+
+}  // namespace
+
+struct gemm_plan {
+    int device = 0;
+    int sm_count = 0;
+    int max_ctas[3] = {0, 0, 0};  // resident CTAs for pair = 1, 2 (index by pair)
+    int pair = 2;
+    int group_m = 0;
+    int cap_ctas = 0;
+    int* d_status = nullptr;      // 4 ints, see Params::status
+    int last_grid = 0;
+    std::mutex host_mu;           // serialises gemm_plan_run_host's buffers
+    void* hbuf[3] = {nullptr, nullptr, nullptr};
+    size_t hcap[3] = {0, 0, 0};
+};
+
+namespace {
+
+// Pure host checks, no CUDA call: shared by every run entry point.
+int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype) {
+    if (dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    if (C == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0) return GEMM_ERR_MISALIGNED;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0))
+        return GEMM_ERR_MISALIGNED;
+    if ((K * 2) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    if ((N * elem_bytes(out_dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;
+}
+
+int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
+           int out_dtype, cudaStream_t stream) {
+    if (K == 0) {
+        const size_t n16 = (size_t)M * (size_t)N * elem_bytes(out_dtype) / 16;
+        const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)plan->sm_count * 8);
+        fill_zero_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(reinterpret_cast<uint4*>(C), n16);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+    const int pair = plan->pair;
+    const int tile_m = kRowsPerCta * pair;
+    Params p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.tiles_m = (int)((M + tile_m - 1) / tile_m);
+    p.tiles_n = (int)((N + kTileN - 1) / kTileN);
+    p.k_blocks = (int)((K + kBlockK - 1) / kBlockK);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = plan->group_m > 0 ? plan->group_m : 8;
+    p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+    p.idesc = make_idesc(dtype, tile_m, kTileN);
+    p.status = plan->d_status;
+
+    CUtensorMap tmA, tmB, tmC;
+    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (rc == GEMM_OK)
+        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(kTileN / pair), kBlockK,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (rc == GEMM_OK)
+        rc = encode_2d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, 32, (uint32_t)(128 / elem_bytes(out_dtype)),
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc != GEMM_OK) return rc;
+
+    int units = plan->max_ctas[pair] / pair;
+    if (plan->cap_ctas > 0) units = std::min(units, std::max(1, plan->cap_ctas / pair));
+    units = std::max(1, std::min(units, p.num_tiles));
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * pair), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes(pair);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pick_kernel(pair, out_dtype), tmA, tmB, tmC, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    plan->last_grid = units * pair;
+    return GEMM_OK;
+}
+
+int query_capacity(gemm_plan* plan, int pair) {
+    for (int out = 0; out < 3; ++out) {
+        if (cudaFuncSetAttribute(pick_kernel(pair, out), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes(pair)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (pair == 2 &&
+            cudaFuncSetAttribute(pick_kernel(pair, out), cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+                cudaSuccess) {
+            cudaGetLastError();
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(plan->sm_count / pair * pair), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes(pair);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, pick_kernel(pair, GEMM_BF16), &cfg) != cudaSuccess ||
+        clusters <= 0) {
+        cudaGetLastError();
+        clusters = plan->sm_count / pair;  // one CTA per SM is what the shared-memory budget allows
+    }
+    plan->max_ctas[pair] = clusters * pair;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
+    if (out == nullptr || flags != 0u) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (device < 0 && cudaGetDevice(&device) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (device >= count || device >= kMaxDevices) return GEMM_ERR_INVALID_ARG;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_NO_DEVICE;  // built for sm_103a only
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (cudaSetDevice(device) != cudaSuccess) return GEMM_ERR_CUDA;
+    gemm_plan* plan = new (std::nothrow) gemm_plan();
+    if (!plan) return GEMM_ERR_CUDA;
+    plan->device = device;
+    plan->sm_count = prop.multiProcessorCount;
+    int rc = query_capacity(plan, 1);
+    if (rc == GEMM_OK) rc = query_capacity(plan, 2);
+    if (rc == GEMM_OK && cudaMalloc(&plan->d_status, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMemset(plan->d_status, 0, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc != GEMM_OK) {
+        if (plan->d_status) cudaFree(plan->d_status);
+        delete plan;
+        cudaSetDevice(prev);
+        return rc;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_plans[device].push_back(plan);
+    }
+    cudaSetDevice(prev);
+    *out = plan;
+    return GEMM_OK;
+}
+
+int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    switch (option) {
+        case GEMM_OPT_CTA_PAIR:
+            if (value != 1 && value != 2) return GEMM_ERR_INVALID_ARG;
+            plan->pair = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_GROUP_M:
+            if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+            plan->group_m = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_MAX_CTAS:
+            if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+            plan->cap_ctas = (int)value;
+            return GEMM_OK;
+        default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                  int dtype, int out_dtype, void* stream) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    int rc = validate(A, B, C, M, N, K, dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
+             void* stream) {
+    int rc = validate(A, B, C, M, N, K, dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    gemm_plan* plan = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (dev >= 0 && dev < kMaxDevices && !g_plans[dev].empty()) plan = g_plans[dev].back();
+    }
+    if (!plan) return GEMM_ERR_NO_PLAN;
+    return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host, void* C_host, int64_t M,
+                       int64_t N, int64_t K, int dtype, int out_dtype, void* stream) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    int rc = validate(A_host, B_host, C_host, M, N, K, dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes[3] = {(size_t)M * (size_t)K * 2, (size_t)N * (size_t)K * 2,
+                             (size_t)M * (size_t)N * (size_t)elem_bytes(out_dtype)};
+    std::lock_guard<std::mutex> lk(plan->host_mu);
+    for (int i = 0; i < 3; ++i) {
+        if (bytes[i] > plan->hcap[i]) {
+            if (plan->hbuf[i]) {
+                cudaStreamSynchronize(s);
+                cudaFree(plan->hbuf[i]);
+                plan->hbuf[i] = nullptr;
+                plan->hcap[i] = 0;
+            }
+            if (cudaMalloc(&plan->hbuf[i], bytes[i]) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            plan->hcap[i] = bytes[i];
+        }
+    }
+    if (K > 0) {
+        if (cudaMemcpyAsync(plan->hbuf[0], A_host, bytes[0], cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(plan->hbuf[1], B_host, bytes[1], cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
+    rc = launch(plan, plan->hbuf[0], plan->hbuf[1], plan->hbuf[2], M, N, K, dtype, out_dtype, s);
+    if (rc != GEMM_OK) return rc;
+    if (cudaMemcpyAsync(C_host, plan->hbuf[2], bytes[2], cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+int gemm_plan_status(gemm_plan_t plan, int* device_status) {
+    if (!plan || !device_status) return GEMM_ERR_INVALID_ARG;
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, plan->d_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(plan->d_status, 0, sizeof(h)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    *device_status = h[0];
+    return GEMM_OK;
+}
+
+int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
+    if (!plan || !ctas) return GEMM_ERR_INVALID_ARG;
+    *ctas = plan->last_grid;
+    return GEMM_OK;
+}
+
+int gemm_plan_destroy(gemm_plan_t plan) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (plan->device >= 0 && plan->device < kMaxDevices) {
+            auto& v = g_plans[plan->device];
+            for (size_t i = 0; i < v.size(); ++i)
+                if (v[i] == plan) { v.erase(v.begin() + (long)i); break; }
+        }
+    }
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(plan->device);
+    if (plan->d_status) cudaFree(plan->d_status);
+    for (int i = 0; i < 3; ++i)
+        if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);
+    cudaSetDevice(prev);
+    delete plan;
+    return GEMM_OK;
+}
+
+const char* gemm_strerror(int status) {
+    switch (status) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported shape or pitch (K % 8, N * out_bytes % 16, or size >= 2^31)";
+        case GEMM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case GEMM_ERR_CUDA: return "CUDA runtime call failed";
+        case GEMM_ERR_DRIVER: return "tensor-map encoding failed or driver entry point missing";
+        case GEMM_ERR_NO_PLAN: return "no plan created for the current device";
+        case GEMM_ERR_TIMEOUT: return "a bounded wait in the kernel expired";
+        case GEMM_ERR_NO_DEVICE: return "no usable sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

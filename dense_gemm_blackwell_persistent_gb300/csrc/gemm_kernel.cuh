@@ -1,0 +1,382 @@
+// gemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// C[M×N] = A[M×K] · B[N×K]ᵀ, bf16/f16 in, fp32 accumulate in TMEM, C out as
+// fp32/bf16/f16.  One CTA (or one CTA pair) stays resident per SM (pair of
+// SMs) and walks a static list of output tiles.
+//
+// Roles inside a CTA (192 threads):
+//   warp 0      TMA producer: fills a kStages-deep shared-memory ring with
+//               64-wide K slices of A and B (128-byte swizzle, zero fill
+//               outside the tensor).  Ring slots are guarded by full/empty
+//               mbarriers.
+//   warp 1      allocates TMEM; in the leader CTA one thread issues
+//               tcgen05.mma into one of two TMEM accumulators (2 × 256
+//               columns) and commits completions to the mbarriers.
+//   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging ->
+//               TMA store, while the MMA thread already fills the other
+//               accumulator with the next tile.
+//
+// With kPair == 2 two CTAs of a cluster form one 256×256 tile: each holds its
+// own 128 rows of A and 128 rows (half) of B, the leader issues
+// tcgen05.mma.cta_group::2 with M = 256, and each CTA's TMEM receives its own
+// 128 rows of the result.  This is the collective MMA of "Writing Mosaic GPU
+// kernels with Pallas", "Collective MMA" (A and D per CTA, B split between
+// the pair) with the B halves loaded as partitioned, leader-tracked copies.
+//
+// Design sources on the pages (prior art, restated for this hardware):
+//   * tiles of A (BM×BK) and B (BN×BK) staged in shared memory, loaded by
+//     TMA under an mbarrier with expected bytes, consumed by tcgen05.mma in
+//     K = 16 steps, accumulators in TMEM: "Optimizing Blackwell Matrix
+//     Multiplication in Mojo (Part 2)", "Kernel 2: TMA and Tensor Core".
+//   * 128-byte swizzle, Swizzle<3,4,3>, one box of 64 K elements per row:
+//     same page, "Kernel 3: Swizzling" and "Swizzling math".
+//   * epilogue through swizzled shared memory and TMA stores with commit
+//     groups: same page, "Kernel 4".
+//   * first MMA of a tile overwrites (accumulate flag 0): same page, Kernel 2
+//     code (c_scale 0 on the first MMA).
+//   * multi-slot ring with full/empty barriers and slot refill once the
+//     consumer released it: "Writing Mosaic GPU kernels with Pallas",
+//     "Barrier" and the pipelined Hopper matmul.
+//   * grouped rasterisation for L2 reuse: same reference, "Utilizing L2
+//     cache" (grid reordered as (m // mt, n, mt)).
+//   * persistent grid of one CTA per SM: "Collective matrix multiplication"
+//     (grid = number of SMs).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int kNumThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kBlockK = 64;              // one 128-byte swizzle row of 16-bit elements
+constexpr int kMmaK = 16;                // K of one kind::f16 MMA (32 bytes)
+constexpr int kRowsPerCta = 128;         // TMEM lanes = rows of A per CTA
+constexpr int kTileN = 256;              // accumulator columns per tile
+constexpr int kTmemCols = 2 * kTileN;    // two accumulators
+constexpr int kStageBytesA = kRowsPerCta * kBlockK * 2;
+constexpr int kStagingSlotBytes = 32 * 128;  // one 32-row × 128-byte TMA store box
+constexpr int kStagingBytes = kEpiWarps * 2 * kStagingSlotBytes;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any single wait
+
+constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2;
+constexpr int kErrTimeout = -7;
+
+struct Params {
+    int M, N, K;
+    int tiles_m, tiles_n, k_blocks, num_tiles, group_m;
+    uint32_t idesc;
+    int* status;  // [0] first error code, [1] role, [2] block, [3] detail
+};
+
+template <int kPair>
+struct Cfg {
+    static constexpr int kTileM = kRowsPerCta * kPair;          // rows per (pair) tile
+    static constexpr int kRowsB = kTileN / kPair;               // B rows held per CTA
+    static constexpr int kStageBytesB = kRowsB * kBlockK * 2;
+    static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+    static constexpr int kStages = kPair == 2 ? 6 : 4;
+    static constexpr int kOffB = kStages * kStageBytesA;
+    static constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
+    static constexpr int kOffBars = kOffStaging + kStagingBytes;
+    static constexpr int kNumBars = 2 * kStages + 4;
+    static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + slack to align the base
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
+    static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // both CTAs' copies land on the leader
+};
+
+// tcgen05 shared-memory matrix descriptor for a K-major tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address / 16
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused when swizzled)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: 8 rows × 128 B
+    d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                     // layout: 128-byte swizzle
+    return d;
+}
+
+// Output tile of linear tile index t: groups of `group_m` tile rows are
+// walked column by column, so the tiles in flight at once share rows of A
+// and columns of Bᵀ in L2.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mt, int& nt) {
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int gsize = min(p.tiles_m - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mt = first_m + r % gsize;
+    nt = r / gsize;
+}
+
+__device__ __forceinline__ void record_error(const Params& p, int role, int detail) {
+    if (atomicCAS(p.status, 0, kErrTimeout) == 0) {
+        p.status[1] = role;
+        p.status[2] = (int)blockIdx.x;
+        p.status[3] = detail;
+    }
+}
+
+// Wait for the phase of parity `parity` of `bar`, for at most kWaitLimitNs.
+// Returns false (and raises the CTA's abort flag) if the bound expires or
+// another role of this CTA has already aborted.
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             const Params& p, int role, int detail) {
+    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(p, role, detail);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
+    if (out == kOutBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <int kPair, int kOut>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_tn_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const Params p) {
+    using C = Cfg<kPair>;
+    constexpr int kStages = C::kStages;
+    constexpr int kChunkCols = kOut == kOutF32 ? 32 : 64;   // columns per 128-byte store box
+    constexpr int kChunks = kTileN / kChunkCols;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+
+    const uint32_t bars = base + C::kOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kPair == 2 ? cluster_cta_rank() : 0u;
+    const int pair_id = kPair == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int num_pairs = kPair == 2 ? (int)num_clusters_x() : (int)gridDim.x;
+
+    // ---- set-up: barriers, TMEM, tensor-map prefetch
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), kEpiWarps * kPair);
+        }
+        *abort_flag = 0;
+        fence_mbar_init_cluster();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc<kPair>(smem_addr(tmem_holder), kTmemCols);
+        tmem_relinquish<kPair>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (kPair == 2) {
+        cluster_arrive();
+        cluster_wait();
+    }
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int t = pair_id; t < p.num_tiles && ok; t += num_pairs) {
+                int mt, nt;
+                tile_coords(p, t, mt, nt);
+                const int a_row = mt * C::kTileM + (int)rank * kRowsPerCta;
+                const int b_row = nt * kTileN + (int)rank * C::kRowsB;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
+                    const uint32_t a_dst = base + stage * kStageBytesA;
+                    const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
+                    if constexpr (kPair == 2) {
+                        const uint32_t fb_leader = map_shared_rank(fb, 0);
+                        tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
+                        tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * kBlockK, b_row);
+                    } else {
+                        tma_load_2d(a_dst, &tmA, fb, kb * kBlockK, a_row);
+                        tma_load_2d(b_dst, &tmB, fb, kb * kBlockK, b_row);
+                    }
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Every slot's last use must be released (the MMA's commit arrives
+            // on this CTA's empty barriers) before the CTA may exit.
+            for (int s = 0; s < kStages && ok; ++s) {
+                ok = wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 1, s);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer (leader CTA only)
+        if (rank == 0 && lane == 0) {
+            const uint32_t a_base = base, b_base = base + C::kOffB;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int t = pair_id; t < p.num_tiles && ok; t += num_pairs, ++i) {
+                const uint32_t b = i & 1, aphase = (i >> 1) & 1;
+                if (!wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * kTileN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded<false>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
+                    const uint64_t bd = smem_desc_sw128(b_base + stage * C::kStageBytesB);
+#pragma unroll
+                    for (int j = 0; j < kBlockK / kMmaK; ++j) {
+                        // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
+                        tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, (kb | j) != 0);
+                    }
+                    if constexpr (kPair == 2) tc_commit_pair(empty_bar(stage), 0x3);
+                    else tc_commit(empty_bar(stage));
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), 0x3);
+                else tc_commit(accf_bar(b));
+            }
+            // Both accumulators must be released by every epilogue warp of the
+            // pair (the peer's arrive on this CTA's barriers) before exit.
+            for (int j = 0; j < 2 && ok; ++j, ++i) {
+                ok = wait_bounded<true>(acce_bar(i & 1), ((i >> 1) & 1) ^ 1u, abort_flag, p, 4, j);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue warps
+        const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad+31
+        const uint32_t staging = base + C::kOffStaging + (uint32_t)(warp - 2) * 2u * kStagingSlotBytes;
+        uint32_t slot = 0;
+        int i = 0;
+        for (int t = pair_id; t < p.num_tiles; t += num_pairs, ++i) {
+            const uint32_t b = i & 1, aphase = (i >> 1) & 1;
+            const bool got = wait_bounded<false>(accf_bar(b), aphase, abort_flag, p, 5, i);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after_sync();
+            int mt, nt;
+            tile_coords(p, t, mt, nt);
+            const int row0 = mt * C::kTileM + (int)rank * kRowsPerCta + quad * 32;
+            const int col0 = nt * kTileN;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kTileN;
+            if (row0 < p.M) {
+                for (int c = 0; c < kChunks; ++c) {
+                    const int ccol = col0 + c * kChunkCols;
+                    if (ccol >= p.N) break;
+                    uint32_t packed[32];
+                    if constexpr (kOut == kOutF32) {
+                        tmem_ld_32x32b_x32(t_row + c * kChunkCols, packed);
+                        tmem_ld_wait();
+                    } else {
+                        uint32_t lo[32], hi[32];
+                        tmem_ld_32x32b_x32(t_row + c * kChunkCols, lo);
+                        tmem_ld_32x32b_x32(t_row + c * kChunkCols + 32, hi);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            packed[q] = pack2(__uint_as_float(lo[2 * q]), __uint_as_float(lo[2 * q + 1]), kOut);
+                            packed[16 + q] = pack2(__uint_as_float(hi[2 * q]), __uint_as_float(hi[2 * q + 1]), kOut);
+                        }
+                    }
+                    const uint32_t buf = staging + (slot & 1u) * kStagingSlotBytes;
+                    ++slot;
+                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
+                    __syncwarp();
+                    // Row `lane` of a 32×128-byte box, 16-byte chunk q stored at
+                    // chunk q ^ (row % 8): the 128-byte swizzle the TMA store undoes.
+                    const uint32_t row_addr = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        st_shared_v4(row_addr + (((uint32_t)q ^ ((uint32_t)lane & 7u)) << 4), packed[4 * q],
+                                     packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, ccol, row0);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (kPair == 2) mbar_arrive_cluster(map_shared_rank(acce_bar(b), 0));
+                else mbar_arrive_local(acce_bar(b));
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        // A bounded wait gave up: let copies and MMAs already in flight land
+        // (they finish in microseconds) before TMEM and shared memory go away.
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 2000000ull) { }
+        }
+        __syncthreads();
+    }
+    if constexpr (kPair == 2) {
+        cluster_arrive();
+        cluster_wait();
+    }
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<kPair>(tmem_base, kTmemCols);
+    }
+}
+
+// C = 0 for K == 0 (the empty sum).  `n16` 16-byte words.
+__global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        c[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+}  // namespace gb300

@@ -1,0 +1,123 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Operation.  C = A·Bᵀ: A is M×K row-major, B is stored transposed as N×K
+ * row-major, C is M×N row-major.  Inputs are bf16 or f16 (both the same
+ * type), products are accumulated in fp32, and C is written as fp32, bf16 or
+ * f16 (rounded to nearest, ties to even).  This is the problem statement of
+ * "Optimizing Blackwell Matrix Multiplication in Mojo (Part 2)" (intro and
+ * "Kernel 2: TMA and Tensor Core": B kept N×K so that both operands are read
+ * along K), with the bf16-in / fp32-accumulate / cast-once-at-the-end
+ * precision of "Chapter 7: Writing Custom Kernels with Pallas", §4.1'.
+ *
+ * Device.  Everything runs on one GB300 GPU.  A, B and C are device pointers
+ * owned by the caller; the library never allocates, frees or retains them.
+ * Work is enqueued asynchronously on the caller's stream (a cudaStream_t,
+ * passed as void* so that this header needs no CUDA header); 0 means the
+ * legacy default stream.
+ *
+ * Layout rules (checked on the host before anything is launched):
+ *   - A, B, C 16-byte aligned;
+ *   - K * 2 bytes and N * sizeof(C element) bytes multiples of 16, i.e.
+ *     K % 8 == 0 and N % 8 == 0 (bf16/f16 out) or N % 4 == 0 (fp32 out);
+ *   - M, N, K < 2^31.
+ * Other shapes return GEMM_ERR_UNSUPPORTED: there is no slow fallback path.
+ *
+ * Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 writes C = 0 (the
+ * empty sum) with a small fill kernel.
+ *
+ * Errors.  Every entry point returns a gemm_status_t.  Problems visible on
+ * the host (bad arguments, alignment, a CUDA or driver call failing) are
+ * returned at once and nothing is enqueued.  A wait inside the kernel that
+ * outlives its bound (about two seconds; it never does in a correct run)
+ * makes the kernel record GEMM_ERR_TIMEOUT in the plan's device status word
+ * and return early; gemm_plan_status() reads that word after the caller has
+ * synchronised the stream.
+ *
+ * Threads.  A plan may be used from several host threads and streams at
+ * once; calls build their tensor maps on the host stack and share only
+ * read-only plan state plus the device status word.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad dtype pair, bad option */
+    GEMM_ERR_UNSUPPORTED = -2,   /* shape/pitch TMA cannot address (see layout rules)       */
+    GEMM_ERR_MISALIGNED = -3,    /* a pointer not 16-byte aligned                            */
+    GEMM_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute, copy)     */
+    GEMM_ERR_DRIVER = -5,        /* the driver's tensor-map encoder failed or is missing     */
+    GEMM_ERR_NO_PLAN = -6,       /* gemm_run with no plan created for the current device     */
+    GEMM_ERR_TIMEOUT = -7,       /* device side: a bounded wait expired (see gemm_plan_status) */
+    GEMM_ERR_NO_DEVICE = -8      /* no usable sm_103 device                                   */
+} gemm_status_t;
+
+typedef struct gemm_plan* gemm_plan_t;
+
+/* Plan options (gemm_plan_set_option).  For tuning sweeps and tests; the
+ * defaults are what the library picks itself. */
+typedef enum {
+    GEMM_OPT_CTA_PAIR = 1,       /* 2 (default): 2-CTA pairs, 256×256 tile per pair;
+                                    1: one CTA per 128×256 tile                         */
+    GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
+    GEMM_OPT_MAX_CTAS = 3        /* cap on resident CTAs of the persistent grid (0 = all SMs) */
+} gemm_option_t;
+
+/* Create a plan for `device` (-1 = the current device); it becomes the plan
+ * gemm_run() uses on that device while it is the newest one alive.  Queries the SM count and the resident
+ * cluster capacity, sets kernel attributes and allocates one 4-byte device
+ * status word (the only device memory the library owns).  `flags` must be 0.
+ * The caller owns the plan and frees it with gemm_plan_destroy(). */
+int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
+
+/* Set a plan option (see gemm_option_t).  Not thread-safe with concurrent
+ * runs on the same plan. */
+int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value);
+
+/* C = A·Bᵀ on `stream` with the most recently created plan of the current
+ * device that is still alive (GEMM_ERR_NO_PLAN if none).  dtype: GEMM_BF16 or GEMM_F16 (A and B);
+ * out_dtype: GEMM_F32, GEMM_BF16 or GEMM_F16.  Asynchronous. */
+int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+             int dtype, int out_dtype, void* stream);
+
+/* Same, with an explicit plan.  The plan's device must be current. */
+int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
+                  int64_t N, int64_t K, int dtype, int out_dtype, void* stream);
+
+/* End-to-end form for callers whose operands live in host memory: copies A
+ * and B (host, ideally pinned) to device buffers the plan owns (grown on
+ * demand and kept for reuse), runs the product, copies C back to host
+ * memory, and synchronises `stream` before returning.  Same shape rules. */
+int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host, void* C_host,
+                       int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, void* stream);
+
+/* Read and clear the plan's device status word.  Synchronises the device.
+ * *device_status receives GEMM_OK or the first device-side error code
+ * recorded since the last call. */
+int gemm_plan_status(gemm_plan_t plan, int* device_status);
+
+/* Number of CTAs the last run on this plan launched (for reports). */
+int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
+
+/* Free the plan.  The caller must have synchronised every stream that still
+ * runs work of this plan.  gemm_run() then uses the newest remaining plan of
+ * the device, or returns GEMM_ERR_NO_PLAN if none is left. */
+int gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static text for a status code. */
+const char* gemm_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

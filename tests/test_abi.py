@@ -1,0 +1,103 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/*.h declares, and rejects bad arguments on the host before any CUDA
+call.  No compute calls are made here."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "while", "for", "return", "sizeof"):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    entry.build()
+    import dense_gemm_blackwell_persistent_gb300 as g
+    return g
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_plan_run", "gemm_strerror"):
+        assert required in names, names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_library_is_native_sm103a(lib):
+    data = open(lib.LIB_PATH, "rb").read()
+    assert b"sm_103a" in data or b"sm_103" in data
+
+
+def test_host_validation_without_gpu(lib):
+    vp = ctypes.c_void_p
+    rs = lib.raw_status
+    good = vp(1 << 20)
+    # bad dtype pair
+    assert rs("gemm_run", good, good, good, 64, 64, 64, 2, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_run", good, good, good, 64, 64, 64, 0, 7, None) == lib.GEMM_ERR_INVALID_ARG
+    # negative sizes
+    assert rs("gemm_run", good, good, good, -1, 64, 64, 0, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    # null pointers
+    assert rs("gemm_run", None, good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_run", good, good, None, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    # misaligned pointers
+    assert rs("gemm_run", vp((1 << 20) + 8), good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_MISALIGNED
+    assert rs("gemm_run", good, good, vp((1 << 20) + 4), 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_MISALIGNED
+    # pitches TMA cannot address
+    assert rs("gemm_run", good, good, good, 64, 64, 60, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_run", good, good, good, 64, 6, 64, 0, 0, None) == lib.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_run", good, good, good, 64, 2, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_run", good, good, good, 1 << 31, 64, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+    # empty problems are a no-op and touch nothing
+    assert rs("gemm_run", None, None, None, 0, 64, 64, 0, 2, None) == lib.GEMM_OK
+    assert rs("gemm_run", None, None, None, 64, 0, 64, 0, 2, None) == lib.GEMM_OK
+    # null plan handles
+    assert rs("gemm_plan_run", None, good, good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_destroy", None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_set_option", None, 1, ctypes.c_int64(2)) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_create", None, -1, 0) == lib.GEMM_ERR_INVALID_ARG
+    for code in range(-8, 1):
+        assert lib.gemm_strerror(code) != "unknown status"
+
+
+def test_no_device_is_reported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(lib.GemmError) as e:
+        lib.gemm_plan_create(-1)
+    assert e.value.status == lib.GEMM_ERR_NO_DEVICE
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)
+    # a well-formed call with no device: fails cleanly, enqueues nothing
+    assert lib.raw_status("gemm_run", good, good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_NO_DEVICE
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle and has no Python arithmetic path."""
+    pkg = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True) + \
+            glob.glob(os.path.join(pkg, "csrc", "*")):
+        text = open(path).read()
+        assert "oracle" not in text.replace("oracle/", ""), path
+        assert "import numpy" not in text, path

@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every test here needs a GB300 and is marked ``gpu``.  Inputs come from the
+seeded generators in workloads.py; expected values come only from oracle/.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+OUTS = [wl.F32, wl.BF16, wl.F16]
+TORCH = wl.TORCH_DTYPES
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_gemm_blackwell_persistent_gb300 as g
+    return g
+
+
+@pytest.fixture(scope="module")
+def plan(g):
+    torch.cuda.set_device(0)
+    h = g.gemm_plan_create(0)
+    yield h
+    torch.cuda.synchronize()
+    g.gemm_plan_destroy(h)
+
+
+@pytest.fixture
+def fresh_plan(g):
+    torch.cuda.set_device(0)
+    h = g.gemm_plan_create(0)
+    yield h
+    torch.cuda.synchronize()
+    g.gemm_plan_destroy(h)
+
+
+def run(g, plan, A, B, out_dtype, C=None):
+    """C = A·Bᵀ through gemm_plan_run; C is poisoned with NaN first."""
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.full((M, N), float("nan"), dtype=TORCH[out_dtype], device="cuda")
+    code = wl.BF16 if A.dtype == torch.bfloat16 else wl.F16
+    g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, code, out_dtype,
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+    return C
+
+
+def oracle_full(A, B):
+    dt = wl.BF16 if A.dtype == torch.bfloat16 else wl.F16
+    return oracle.gemm(wl.as_bits(A), wl.as_bits(B), dt)
+
+
+def draw(M, N, K, dtype=wl.BF16, dist="normal", seed=0):
+    w = wl.Workload("case", M, N, K, dtype, wl.F32, dist, seed,
+                    lo=-4 if dist == "int" else -1.0, hi=4 if dist == "int" else 1.0)
+    return wl.make_inputs(w)
+
+
+# ------------------------------------------------------------------ bit-exact integer runs
+
+@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("out", OUTS)
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 264), (384, 512, 1024)])
+def test_integer_inputs_bit_exact(g, plan, pair, out, shape):
+    M, N, K = shape
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, pair)
+    try:
+        A, B = draw(M, N, K, dist="int", seed=0)
+        C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), out))
+        C_ref, _ = oracle_full(A, B)
+        if out == wl.F32:
+            want = C_ref
+        else:
+            want = oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(C, want), f"{int((C != want).sum())} mismatches"
+    finally:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 2)
+
+
+def test_integer_workload_256(g, plan):
+    w = wl.WORKLOADS["gemm_256_int"]
+    A, B = wl.make_inputs(w)
+    C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), w.out_dtype))
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(C, C_ref)
+
+
+# ------------------------------------------------------------------ random inputs, full comparison
+
+def test_workload_256_f32out(g, plan):
+    w = wl.WORKLOADS["gemm_256_f32out"]
+    A, B = wl.make_inputs(w)
+    C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), w.out_dtype))
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(C, C_ref, S, w.out_dtype, w.name)
+
+
+SHAPES = [
+    (8, 8, 8), (1, 8, 16), (3, 16, 24), (128, 256, 64), (129, 264, 72), (255, 248, 136),
+    (256, 256, 128), (257, 264, 200), (384, 520, 1000), (1000, 776, 520), (640, 1288, 64),
+]
+
+
+@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_shape_sweep(g, plan, pair, shape):
+    M, N, K = shape
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, pair)
+    try:
+        for i, out in enumerate(OUTS):
+            dtype = wl.BF16 if (i + M) % 2 == 0 else wl.F16
+            A, B = draw(M, N, K, dtype=dtype, seed=M * 7 + N * 3 + K + i)
+            C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), out))
+            C_ref, S = oracle_full(A, B)
+            parity.assert_within(C, C_ref, S, out, f"{shape} pair={pair} out={out} in={dtype}")
+    finally:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 2)
+
+
+@pytest.mark.parametrize("pair,ctas,group", [(2, 2, 8), (2, 6, 3), (1, 1, 8), (1, 5, 1), (2, 4, 1)])
+def test_persistent_loop_many_tiles(g, fresh_plan, pair, ctas, group):
+    """Few resident CTAs, many tiles each: wraps the shared-memory ring many
+    times and alternates both TMEM accumulators across tiles."""
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, ctas)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_GROUP_M, group)
+    M, N, K = 1100, 1288, 328
+    for out in OUTS:
+        A, B = draw(M, N, K, seed=ctas * 10 + group + out)
+        C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
+        assert g.gemm_plan_last_grid(fresh_plan) == ctas // pair * pair
+        C_ref, S = oracle_full(A, B)
+        parity.assert_within(C, C_ref, S, out, f"pair={pair} ctas={ctas} group={group} out={out}")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full_size_sampled(g, plan, name):
+    """Full size, default launch configuration (the one the benchmark times):
+    every element written and finite, sampled entries against the oracle."""
+    w = wl.WORKLOADS[name]
+    A, B = wl.make_inputs(w)
+    C = run(g, plan, A.cuda(), B.cuda(), w.out_dtype)
+    assert bool(torch.isfinite(C).all()), "unwritten (NaN-poisoned) or non-finite outputs"
+    I, J = parity.sample_positions(w.M, w.N, 4096, seed=w.seed)
+    C_ref, S = oracle.gemm_entries(wl.as_bits(A), wl.as_bits(B), w.dtype, I, J)
+    got = parity.to_f64(C)[I, J]
+    parity.assert_within(got, C_ref, S, w.out_dtype, name)
+
+
+def test_medium_ragged_full(g, plan):
+    """The ragged workload's distribution and dtype, at a size the oracle
+    finishes in seconds: several tiles in each direction, ragged in M, N and K."""
+    w = wl.WORKLOADS["gemm_ragged_4000x3000x5000"]
+    A, B = wl.make_inputs(w, M=1000, N=760, K=1256, seed=33)
+    C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), w.out_dtype))
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(C, C_ref, S, w.out_dtype, "ragged 1000x760x1256")
+
+
+# ------------------------------------------------------------------ edges and API behaviour
+
+def test_k_zero_writes_zeros(g, plan):
+    for out in OUTS:
+        A = torch.empty((37, 0), dtype=torch.bfloat16, device="cuda")
+        B = torch.empty((48, 0), dtype=torch.bfloat16, device="cuda")
+        C = run(g, plan, A, B, out)
+        assert bool((C == 0).all())
+
+
+def test_m_or_n_zero_is_noop(g, plan):
+    A = torch.randn(0, 64, device="cuda").to(torch.bfloat16)
+    B = torch.randn(16, 64, device="cuda").to(torch.bfloat16)
+    C = torch.empty((0, 16), dtype=torch.float32, device="cuda")
+    run(g, plan, A, B, wl.F32, C)
+    A = torch.randn(16, 64, device="cuda").to(torch.bfloat16)
+    sentinel = torch.full((4,), 7.0, device="cuda")
+    g.gemm_plan_run(plan, A.data_ptr(), A.data_ptr(), sentinel.data_ptr(), 16, 0, 64, 0, 2, 0)
+    torch.cuda.synchronize()
+    assert bool((sentinel == 7.0).all())
+
+
+def test_rows_beyond_m_untouched(g, plan):
+    """C buffer has extra NaN rows past M: the clipped stores must not reach them."""
+    M, N, K = 300, 264, 136
+    A, B = draw(M, N, K, seed=5)
+    for out in OUTS:
+        buf = torch.full((M + 3, N), float("nan"), dtype=TORCH[out], device="cuda")
+        run(g, plan, A.cuda(), B.cuda(), out, C=buf)
+        assert bool(torch.isnan(buf[M:]).all())
+        assert bool(torch.isfinite(buf[:M]).all())
+
+
+def test_error_codes(g, plan):
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    rs = g.raw_status
+    import ctypes
+    vp = ctypes.c_void_p
+    p = vp(plan)
+    assert rs("gemm_plan_run", p, vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr() + 4), 64, 64, 64, 0, 2,
+              None) == g.GEMM_ERR_MISALIGNED
+    assert rs("gemm_plan_run", p, vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()), 64, 64, 60, 0, 2,
+              None) == g.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_plan_run", p, vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()), 64, 6, 64, 0, 0,
+              None) == g.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_plan_run", p, vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()), 64, 64, 64, 2, 2,
+              None) == g.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_run", p, vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()), -1, 64, 64, 0, 2,
+              None) == g.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_set_option", p, 1, ctypes.c_int64(3)) == g.GEMM_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+
+
+def test_implicit_plan_and_host_entry_agree(g, plan):
+    M, N, K = 520, 776, 392
+    A, B = draw(M, N, K, dtype=wl.F16, seed=9)
+    C1 = run(g, plan, A.cuda(), B.cuda(), wl.BF16)
+    # gemm_run uses the plan most recently created on the device
+    C2 = torch.full_like(C1, float("nan"))
+    Ad, Bd = A.cuda(), B.cuda()
+    g.gemm_run(Ad.data_ptr(), Bd.data_ptr(), C2.data_ptr(), M, N, K, wl.F16, wl.BF16,
+               torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    # host buffers in, host buffer out
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    C3 = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    g.gemm_plan_run_host(plan, Ah.data_ptr(), Bh.data_ptr(), C3.data_ptr(), M, N, K, wl.F16, wl.BF16,
+                         torch.cuda.current_stream().cuda_stream)
+    assert torch.equal(C1.cpu().view(torch.int16), C3.view(torch.int16))
+
+
+def test_deterministic(g, plan):
+    w = wl.WORKLOADS["gemm_1024x4096x4096_f16"]
+    A, B = wl.make_inputs(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = run(g, plan, Ad, Bd, w.out_dtype)
+    C2 = run(g, plan, Ad, Bd, w.out_dtype)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+def test_torch_matmul_helper(g, plan):
+    A, B = draw(256, 512, 128, seed=3)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = g.matmul(Ad, Bd, out_dtype=torch.float32, plan=plan)
+    torch.cuda.synchronize()
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(parity.to_f64(C), C_ref, S, wl.F32, "matmul helper")
