@@ -47,12 +47,13 @@ _lib.gemm_plan_set_option.argtypes = [_vp, _int, _i64]
 _lib.gemm_run.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
-for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_plan_run",
+for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
 
@@ -86,6 +87,14 @@ def gemm_plan_set_option(plan: int, option: int, value: int) -> None:
 def gemm_run(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int, out_dtype: int,
              stream: int = 0) -> None:
     _check(_lib.gemm_run(_vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, _vp(stream)), "gemm_run")
+
+
+def gemm_run_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int, out_dtype: int,
+                     stream: int = 0) -> None:
+    """Allocation-free gemm_run: for callers that may not allocate device memory
+    (inside CUDA-graph capture, fixed memory pools, foreign allocators)."""
+    _check(_lib.gemm_run_noalloc(_vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, _vp(stream)),
+           "gemm_run_noalloc")
 
 
 def gemm_plan_run(plan: int, A: int, B: int, C: int, M: int, N: int, K: int, dtype: int,

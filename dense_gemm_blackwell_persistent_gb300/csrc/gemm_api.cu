@@ -412,3 +412,94 @@ const char* gemm_strerror(int status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers may not allocate device memory at all: code that runs while a
+// stream is being captured into a CUDA graph (cudaMalloc is not a stream
+// operation and breaks or invalidates the capture), services that reserve
+// every byte of HBM for their own pool at start-up and forbid allocations
+// afterwards, and embedders whose memory is owned by another allocator that
+// must see every device allocation.  gemm_plan_create() allocates the plan's
+// 16-byte status record with cudaMalloc, so those callers use
+// gemm_run_noalloc() instead.  It launches the same kernel, but the kernel's
+// only scratch -- the status record its bounded waits write on timeout --
+// lives in the file-scope array below, which the library's module reserves
+// on every GPU that loads it until the process exits.
+//
+// Limits and sharing: the array holds kNoallocScratchBytes (256 bytes); the
+// kernel needs 16 of them for any M, N, K, and a request beyond the array is
+// rejected with GEMM_ERR_UNSUPPORTED.  Every call on a device shares the same
+// array and it keeps the last call's contents, so each call first clears the
+// status record on its stream; calls that overlap on the GPU (different
+// streams, no ordering between them) race on that record.  The record is not
+// read back by this entry point: device-side timeouts are reported only by
+// the plan path (gemm_plan_status).
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+struct NoallocDevice {
+    std::once_flag once;
+    int rc = GEMM_OK;
+    gemm_plan state;   // host-side launch parameters only; d_status points into the static array
+};
+NoallocDevice g_noalloc[kMaxDevices];
+
+// Bytes of scratch one launch of the kernel needs: its status record.  It
+// does not depend on the problem size.
+size_t noalloc_scratch_bytes(int64_t, int64_t, int64_t) { return 4 * sizeof(int); }
+
+// Once per device, with that device current: fetch the array's device
+// address (a host-side reference to g_noalloc_scratch is only a stand-in and
+// must never reach a kernel) and query the launch capacity.  No allocation.
+void noalloc_setup(NoallocDevice* d, int device) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+        cudaGetLastError();
+        d->rc = GEMM_ERR_CUDA;
+        return;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+        d->rc = GEMM_ERR_NO_DEVICE;
+        return;
+    }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        d->rc = GEMM_ERR_CUDA;
+        return;
+    }
+    d->state.device = device;
+    d->state.sm_count = prop.multiProcessorCount;
+    d->state.d_status = static_cast<int*>(ptr);
+    int rc = query_capacity(&d->state, 1);
+    if (rc == GEMM_OK) rc = query_capacity(&d->state, 2);
+    d->rc = rc;
+}
+
+}  // namespace
+
+extern "C" int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                int dtype, int out_dtype, void* stream) {
+    int rc = validate(A, B, C, M, N, K, dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if (noalloc_scratch_bytes(M, N, K) > kNoallocScratchBytes) return GEMM_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_INVALID_ARG;
+    NoallocDevice* d = &g_noalloc[dev];
+    std::call_once(d->once, noalloc_setup, d, dev);
+    if (d->rc != GEMM_OK) return d->rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(d->state.d_status, 0, noalloc_scratch_bytes(M, N, K), s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return launch(&d->state, A, B, C, M, N, K, dtype, out_dtype, s);
+}

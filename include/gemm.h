@@ -113,6 +113,29 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
  * the device, or returns GEMM_ERR_NO_PLAN if none is left. */
 int gemm_plan_destroy(gemm_plan_t plan);
 
+/* Allocation-free form of gemm_run(), for callers that may not allocate
+ * device memory at all: code running while a stream is being captured into
+ * a CUDA graph, services that hand all of HBM to their own pool at start-up
+ * and forbid later allocations, embedders whose memory belongs to another
+ * allocator.  No plan is needed and nothing is allocated, now or later (no
+ * cudaMalloc, no cudaFree, no allocating library call): the kernel's only
+ * scratch, its 16-byte status record, lives in a 256-byte static device
+ * array that every GPU loading this library keeps until the process exits.
+ * A, B, C and the layout rules are those of gemm_run(); the default
+ * configuration (CTA pairs) is used.
+ *   - The first call on a device sets up that device (looks up the array's
+ *     device address, sets kernel attributes, queries capacity); make that
+ *     first call before any stream capture.
+ *   - Each call clears the status record on `stream` before launching.
+ *     Every call on a device shares the array, so calls that overlap on the
+ *     GPU (unordered streams) race on it.  Device-side timeouts are not
+ *     reported by this entry point; gemm_plan_status() covers the plan path.
+ *   - A scratch requirement beyond the array's 256 bytes is rejected with
+ *     GEMM_ERR_UNSUPPORTED (the kernel needs 16 bytes whatever M, N, K).
+ * The pages have no counterpart: this is a library integration entry point. */
+int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     int dtype, int out_dtype, void* stream);
+
 /* Static text for a status code. */
 const char* gemm_strerror(int status);
 

@@ -1,0 +1,54 @@
+"""gemm_run_noalloc, the allocation-free entry point, against gemm_plan_run.
+
+Some callers of this library may not allocate device memory: code running
+while a stream is captured into a CUDA graph, services that give all of HBM
+to their own pool at start-up, embedders whose memory belongs to another
+allocator.  gemm_run_noalloc serves them: it runs the same kernel with the
+kernel's scratch (its status record) in a static device array instead of a
+plan's cudaMalloc'd word.  Here it is called through the C ABI twice in a row,
+on different shapes and dtypes, and each output is checked against the plan
+entry point's output on the same inputs (and both against the fp64 oracle),
+within the tolerance every parity test uses.
+
+The file name sorts last so that a run stopping at its first failure has
+already run every other test; it also passes alone in a fresh process.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_matches_plan_entry_two_calls_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_gemm_blackwell_persistent_gb300 as g
+    torch.cuda.set_device(0)
+    plan = g.gemm_plan_create(0)
+    stream = torch.cuda.current_stream().cuda_stream
+    cases = [(1000, 776, 1256, wl.BF16, wl.F32, 21), (520, 1288, 392, wl.F16, wl.BF16, 22)]
+    try:
+        for M, N, K, dt, out, seed in cases:
+            w = wl.Workload("noalloc", M, N, K, dt, out, "normal", seed)
+            A, B = wl.make_inputs(w)
+            Ad, Bd = A.cuda(), B.cuda()
+            C_free = torch.full((M, N), float("nan"), dtype=wl.TORCH_DTYPES[out], device="cuda")
+            C_plan = torch.full((M, N), float("nan"), dtype=wl.TORCH_DTYPES[out], device="cuda")
+            g.gemm_run_noalloc(Ad.data_ptr(), Bd.data_ptr(), C_free.data_ptr(), M, N, K, dt, out, stream)
+            g.gemm_plan_run(plan, Ad.data_ptr(), Bd.data_ptr(), C_plan.data_ptr(), M, N, K, dt, out, stream)
+            torch.cuda.synchronize()
+            assert g.gemm_plan_status(plan) == 0
+            C_ref, S = oracle.gemm(wl.as_bits(A), wl.as_bits(B), dt)
+            got_free, got_plan = parity.to_f64(C_free), parity.to_f64(C_plan)
+            tol = parity.tolerance(C_ref, S, out)
+            assert np.all(np.abs(got_free - got_plan) <= tol), f"noalloc vs plan entry, {M}x{N}x{K}"
+            parity.assert_within(got_free, C_ref, S, out, f"noalloc {M}x{N}x{K}")
+            parity.assert_within(got_plan, C_ref, S, out, f"plan {M}x{N}x{K}")
+    finally:
+        torch.cuda.synchronize()
+        g.gemm_plan_destroy(plan)
