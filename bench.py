@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--cta-pair", type=int, default=0, help="force 1 or 2 (0 = library default)")
     ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (0 = library choice)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     return ap.parse_args()
 
@@ -230,6 +231,8 @@ def main():
         g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, args.cta_pair)
     if args.group_m:
         g.gemm_plan_set_option(plan, g.GEMM_OPT_GROUP_M, args.group_m)
+    if args.tile_n:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_TILE_N, args.tile_n)
 
     A_cpu, B_cpu = wl.make_inputs(w)
     A, B = A_cpu.cuda(), B_cpu.cuda()
@@ -346,6 +349,7 @@ def main():
                        "inputs": w.describe(), "parallelism": f"replicas x{world}",
                        "l2": "not flushed" if args.no_flush else "flushed before every step (512 MiB write)",
                        "cta_pair": args.cta_pair or 2, "grid_ctas": g.gemm_plan_last_grid(plan),
+                       "tile": f"{128 * (args.cta_pair or 2)}x{g.gemm_plan_last_tile_n(plan)}x64",
                        "vs_baseline_ref": "pages' 293.6 TFLOP/s, Mojo part-2 kernel 4 on B200 (context)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,

@@ -27,7 +27,7 @@ GEMM_ERR_DRIVER = -5
 GEMM_ERR_NO_PLAN = -6
 GEMM_ERR_TIMEOUT = -7
 GEMM_ERR_NO_DEVICE = -8
-GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS = 1, 2, 3
+GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N = 1, 2, 3, 4
 
 LIB_PATH = _build.LIB
 
@@ -50,11 +50,13 @@ _lib.gemm_plan_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, 
 _lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.gemm_plan_last_tile_n.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
-              "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_destroy"):
+              "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
+              "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
 
 
@@ -118,6 +120,12 @@ def gemm_plan_status(plan: int) -> int:
 def gemm_plan_last_grid(plan: int) -> int:
     n = _int(0)
     _check(_lib.gemm_plan_last_grid(_vp(plan), ctypes.byref(n)), "gemm_plan_last_grid")
+    return n.value
+
+
+def gemm_plan_last_tile_n(plan: int) -> int:
+    n = _int(0)
+    _check(_lib.gemm_plan_last_tile_n(_vp(plan), ctypes.byref(n)), "gemm_plan_last_tile_n")
     return n.value
 
 

@@ -1,7 +1,8 @@
 """Build the CUDA library in-tree with nvcc (sm_103a only).
 
 Produces ``dense_gemm_blackwell_persistent_gb300/_lib/libgb300gemm.so`` from
-``csrc/gemm_api.cu`` (which includes the kernel and PTX headers).  The CUDA
+``csrc/gemm_api.cu`` (host side) and six objects of ``csrc/kernels_inst.cu``
+(one per CTA pairing × output type), compiled in parallel.  The CUDA
 runtime is linked statically and the driver's tensor-map encoder is looked up
 at run time, so the library loads on a machine without a GPU.
 """
@@ -22,7 +23,7 @@ LIB = os.path.join(LIBDIR, "libgb300gemm.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
 
@@ -46,20 +47,47 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
+# (pairing, output type) variants of the kernel, one object file each
+VARIANTS = [(pair, out) for pair in (1, 2) for out in (0, 1, 2)]
+
+
+def _compile(args):
+    cmd, verbose = args
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    return res.stdout + res.stderr if verbose else ""
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit in parallel, then link the shared library."""
+    from concurrent.futures import ThreadPoolExecutor
+
     if not force and up_to_date():
         return LIB
     os.makedirs(LIBDIR, exist_ok=True)
+    objdir = os.path.join(LIBDIR, f"obj{os.getpid()}")
+    os.makedirs(objdir, exist_ok=True)
+    nvcc = _nvcc()
+    common = [nvcc, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c"]
+    if verbose:
+        common.insert(1, "-Xptxas=-v")
+    jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose)]
+    for pair, out in VARIANTS:
+        obj = os.path.join(objdir, f"kernels_p{pair}_o{out}.o")
+        jobs.append((common + [f"-DGEMM_INST_PAIR={pair}", f"-DGEMM_INST_OUT={out}",
+                               os.path.join(CSRC, "kernels_inst.cu"), "-o", obj], verbose))
+    workers = max(1, min(len(jobs), os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        logs = list(ex.map(_compile, jobs))
+    if verbose:
+        print("".join(logs))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, os.path.join(CSRC, "gemm_api.cu"), "-o", tmp]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
-    if verbose:
-        print(res.stdout, res.stderr)
+    objs = sorted(os.path.join(objdir, f) for f in os.listdir(objdir) if f.endswith(".o"))
+    link = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
+    _compile((link, False))
     os.replace(tmp, LIB)
+    shutil.rmtree(objdir, ignore_errors=True)
     return LIB
 
 

@@ -20,6 +20,7 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "kernel_table.h"
 
 namespace {
 
@@ -63,9 +64,9 @@ int get_encoder(EncodeTiledFn* out) {
 }
 
 // Row-major matrix rows×cols (cols contiguous), box = box_rows × box_cols,
-// 128-byte swizzle, zero fill outside the matrix.
+// zero fill outside the matrix.
 int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols, CUtensorMapL2promotion promo) {
+              uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
     EncodeTiledFn enc;
     int rc = get_encoder(&enc);
     if (rc != GEMM_OK) return rc;
@@ -74,30 +75,23 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, tma_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }
-
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
-
-template <int kPair>
-KernelFn kernel_for(int out) {
-    switch (out) {
-        case GEMM_BF16: return gemm_tn_persistent<kPair, kOutBF16>;
-        case GEMM_F16: return gemm_tn_persistent<kPair, kOutF16>;
-        default: return gemm_tn_persistent<kPair, kOutF32>;
-    }
-}
-
-KernelFn pick_kernel(int pair, int out) { return pair == 2 ? kernel_for<2>(out) : kernel_for<1>(out); }
-int smem_bytes(int pair) { return pair == 2 ? Cfg<2>::kSmemBytes : Cfg<1>::kSmemBytes; }
 
 uint32_t make_idesc(int in_dtype, int m, int n) {
     const uint32_t ab = in_dtype == GEMM_BF16 ? 1u : 0u;  // operand format: 0 = f16, 1 = bf16
     return (1u << 4)                   // accumulator format: f32
            | (ab << 7) | (ab << 10)    // A and B formats
            | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);  // both K-major (bits 15/16 = 0)
+}
+
+// C = 0 for K == 0 (the empty sum).  `n16` 16-byte words.
+__global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        c[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace
@@ -109,8 +103,10 @@ struct gemm_plan {
     int pair = 2;
     int group_m = 0;
     int cap_ctas = 0;
+    int tile_n = 0;               // 0 = chosen per problem
     int* d_status = nullptr;      // 4 ints, see Params::status
     int last_grid = 0;
+    int last_tile_n = 0;
     std::mutex host_mu;           // serialises gemm_plan_run_host's buffers
     void* hbuf[3] = {nullptr, nullptr, nullptr};
     size_t hcap[3] = {0, 0, 0};
@@ -135,6 +131,35 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     return GEMM_OK;
 }
 
+// Resident CTA pairs (units) a launch may use.
+int resident_units(const gemm_plan* plan, int pair) {
+    int units = plan->max_ctas[pair] / pair;
+    if (plan->cap_ctas > 0) units = std::min(units, std::max(1, plan->cap_ctas / pair));
+    return std::max(1, units);
+}
+
+// Tile width: the candidate that minimises (waves of resident units) ×
+// (width + a fixed per-tile cost of 32 columns), so that the tile count
+// fills whole waves; ties go to the wider tile.
+int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int pair) {
+    if (plan->tile_n > 0) return plan->tile_n;
+    const int64_t units = resident_units(plan, pair);
+    const int64_t tiles_m = (M + kRowsPerCta * pair - 1) / (kRowsPerCta * pair);
+    int best = kTileWidths[0];
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < kNumTileWidths; ++i) {
+        const int bn = kTileWidths[i];
+        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + units - 1) / units;
+        const int64_t cost = waves * (bn + 32);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
            int out_dtype, cudaStream_t stream) {
     if (K == 0) {
@@ -144,39 +169,42 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
+    const int bn = choose_tile_n(plan, M, N, pair);
+    const KernelInfo ki = kernel_info(pair, bn, out_dtype);
+    if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * pair;
     Params p;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
     p.tiles_m = (int)((M + tile_m - 1) / tile_m);
-    p.tiles_n = (int)((N + kTileN - 1) / kTileN);
+    p.tiles_n = (int)((N + bn - 1) / bn);
     p.k_blocks = (int)((K + kBlockK - 1) / kBlockK);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
-    p.idesc = make_idesc(dtype, tile_m, kTileN);
+    p.idesc = make_idesc(dtype, tile_m, bn);
     p.status = plan->d_status;
 
     CUtensorMap tmA, tmB, tmC;
-    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK,
+    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(kTileN / pair), kBlockK,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / pair), kBlockK,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, 32, (uint32_t)(128 / elem_bytes(out_dtype)),
+        rc = encode_2d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, 32, kChunkCols,
+                       out_dtype == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc != GEMM_OK) return rc;
 
-    int units = plan->max_ctas[pair] / pair;
-    if (plan->cap_ctas > 0) units = std::min(units, std::max(1, plan->cap_ctas / pair));
-    units = std::max(1, std::min(units, p.num_tiles));
+    const int units = std::min(resident_units(plan, pair), p.num_tiles);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * pair), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem_bytes(pair);
+    cfg.dynamicSmemBytes = (size_t)ki.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -185,32 +213,38 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, pick_kernel(pair, out_dtype), tmA, tmB, tmC, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ki.fn, tmA, tmB, tmC, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
     plan->last_grid = units * pair;
+    plan->last_tile_n = bn;
     return GEMM_OK;
 }
 
 int query_capacity(gemm_plan* plan, int pair) {
+    int max_smem = 0;
+    KernelFn probe = nullptr;
     for (int out = 0; out < 3; ++out) {
-        if (cudaFuncSetAttribute(pick_kernel(pair, out), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes(pair)) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_CUDA;
-        }
-        if (pair == 2 &&
-            cudaFuncSetAttribute(pick_kernel(pair, out), cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+        for (int i = 0; i < kNumTileWidths; ++i) {
+            const KernelInfo ki = kernel_info(pair, kTileWidths[i], out);
+            if (ki.fn == nullptr) continue;
+            if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem_bytes) !=
                 cudaSuccess) {
-            cudaGetLastError();
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            if (ki.smem_bytes > max_smem) {
+                max_smem = ki.smem_bytes;
+                probe = ki.fn;
+            }
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(plan->sm_count / pair * pair), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem_bytes(pair);
+    cfg.dynamicSmemBytes = (size_t)max_smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)pair;
@@ -219,8 +253,7 @@ int query_capacity(gemm_plan* plan, int pair) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, pick_kernel(pair, GEMM_BF16), &cfg) != cudaSuccess ||
-        clusters <= 0) {
+    if (probe == nullptr || cudaOccupancyMaxActiveClusters(&clusters, probe, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         clusters = plan->sm_count / pair;  // one CTA per SM is what the shared-memory budget allows
     }
@@ -286,6 +319,18 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
             if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
             plan->cap_ctas = (int)value;
             return GEMM_OK;
+        case GEMM_OPT_TILE_N: {
+            if (value == 0) {
+                plan->tile_n = 0;
+                return GEMM_OK;
+            }
+            for (int i = 0; i < kNumTileWidths; ++i)
+                if (value == kTileWidths[i]) {
+                    plan->tile_n = (int)value;
+                    return GEMM_OK;
+                }
+            return GEMM_ERR_INVALID_ARG;
+        }
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -372,6 +417,12 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status) {
 int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
     if (!plan || !ctas) return GEMM_ERR_INVALID_ARG;
     *ctas = plan->last_grid;
+    return GEMM_OK;
+}
+
+int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
+    if (!plan || !tile_n) return GEMM_ERR_INVALID_ARG;
+    *tile_n = plan->last_tile_n;
     return GEMM_OK;
 }
 

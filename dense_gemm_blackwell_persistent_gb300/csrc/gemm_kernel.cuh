@@ -10,14 +10,18 @@
 //               outside the tensor).  Ring slots are guarded by full/empty
 //               mbarriers.
 //   warp 1      allocates TMEM; in the leader CTA one thread issues
-//               tcgen05.mma into one of two TMEM accumulators (2 × 256
-//               columns) and commits completions to the mbarriers.
+//               tcgen05.mma into one of two TMEM accumulators (columns
+//               0.. and 256.., kBN wide each) and commits completions to
+//               the mbarriers.
 //   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging ->
-//               TMA store, while the MMA thread already fills the other
-//               accumulator with the next tile.
+//               TMA store in 32-column boxes, while the MMA thread already
+//               fills the other accumulator with the next tile.
 //
-// With kPair == 2 two CTAs of a cluster form one 256×256 tile: each holds its
-// own 128 rows of A and 128 rows (half) of B, the leader issues
+// The tile width kBN (256, 224, 192, 160 or 128) is chosen per problem on
+// the host so that the tile count fills whole waves of resident CTA pairs.
+//
+// With kPair == 2 two CTAs of a cluster form one 256×kBN tile: each holds its
+// own 128 rows of A and kBN/2 rows (half) of B, the leader issues
 // tcgen05.mma.cta_group::2 with M = 256, and each CTA's TMEM receives its own
 // 128 rows of the result.  This is the collective MMA of "Writing Mosaic GPU
 // kernels with Pallas", "Collective MMA" (A and D per CTA, B split between
@@ -54,11 +58,10 @@ constexpr int kEpiWarps = 4;
 constexpr int kBlockK = 64;              // one 128-byte swizzle row of 16-bit elements
 constexpr int kMmaK = 16;                // K of one kind::f16 MMA (32 bytes)
 constexpr int kRowsPerCta = 128;         // TMEM lanes = rows of A per CTA
-constexpr int kTileN = 256;              // accumulator columns per tile
-constexpr int kTmemCols = 2 * kTileN;    // two accumulators
+constexpr int kAccStride = 256;          // TMEM columns between the two accumulators
+constexpr int kTmemCols = 2 * kAccStride;
 constexpr int kStageBytesA = kRowsPerCta * kBlockK * 2;
-constexpr int kStagingSlotBytes = 32 * 128;  // one 32-row × 128-byte TMA store box
-constexpr int kStagingBytes = kEpiWarps * 2 * kStagingSlotBytes;
+constexpr int kChunkCols = 32;           // accumulator columns per epilogue store box
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any single wait
 
 constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2;
@@ -71,20 +74,33 @@ struct Params {
     int* status;  // [0] first error code, [1] role, [2] block, [3] detail
 };
 
-template <int kPair>
+// kPair: CTAs per tile (1 or 2); kBN: tile width (accumulator columns, a
+// multiple of 32 up to 256); kOut: C element type.
+template <int kPair, int kBN, int kOut>
 struct Cfg {
+    static_assert(kPair == 1 || kPair == 2, "one CTA or a CTA pair per tile");
+    static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "tile width");
+    static_assert((kBN / kPair) % 8 == 0, "B rows per CTA must fill 1 KB swizzle atoms");
     static constexpr int kTileM = kRowsPerCta * kPair;          // rows per (pair) tile
-    static constexpr int kRowsB = kTileN / kPair;               // B rows held per CTA
+    static constexpr int kRowsB = kBN / kPair;                  // B rows held per CTA
     static constexpr int kStageBytesB = kRowsB * kBlockK * 2;
     static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-    static constexpr int kStages = kPair == 2 ? 6 : 4;
+    static constexpr int kOutBytes = kOut == kOutF32 ? 4 : 2;
+    static constexpr int kRowBytes = kChunkCols * kOutBytes;    // 128 (fp32) or 64 (16-bit)
+    static constexpr int kSlotBytes = 32 * kRowBytes;           // one 32-row store box
+    static constexpr int kStagingBytes = kEpiWarps * 2 * kSlotBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kFixed = kStagingBytes + kBarBytes + 16 + 1024;  // + slack to align the base
+    static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static_assert(kStages >= 3, "ring too shallow");
     static constexpr int kOffB = kStages * kStageBytesA;
     static constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
     static constexpr int kOffBars = kOffStaging + kStagingBytes;
-    static constexpr int kNumBars = 2 * kStages + 4;
-    static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + slack to align the base
+    static constexpr int kOffMisc = kOffBars + kBarBytes;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert((2 * kStages + 4) * 8 <= kBarBytes, "barrier area");
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
     static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // both CTAs' copies land on the leader
 };
@@ -151,14 +167,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
     }
 }
 
-template <int kPair, int kOut>
+template <int kPair, int kBN, int kOut>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tn_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const Params p) {
-    using C = Cfg<kPair>;
+    using C = Cfg<kPair, kBN, kOut>;
     constexpr int kStages = C::kStages;
-    constexpr int kChunkCols = kOut == kOutF32 ? 32 : 64;   // columns per 128-byte store box
-    constexpr int kChunks = kTileN / kChunkCols;
+    constexpr int kChunks = kBN / kChunkCols;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -218,7 +233,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 int mt, nt;
                 tile_coords(p, t, mt, nt);
                 const int a_row = mt * C::kTileM + (int)rank * kRowsPerCta;
-                const int b_row = nt * kTileN + (int)rank * C::kRowsB;
+                const int b_row = nt * kBN + (int)rank * C::kRowsB;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
                         ok = false;
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
                 if (!wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i)) { ok = false; break; }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * kTileN;
+                const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_bounded<false>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
                     tc_fence_after_sync();
@@ -287,7 +302,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     } else {
         // ================= epilogue warps
         const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad+31
-        const uint32_t staging = base + C::kOffStaging + (uint32_t)(warp - 2) * 2u * kStagingSlotBytes;
+        const uint32_t staging = base + C::kOffStaging + (uint32_t)(warp - 2) * 2u * C::kSlotBytes;
         uint32_t slot = 0;
         int i = 0;
         for (int t = pair_id; t < p.num_tiles; t += num_pairs, ++i) {
@@ -298,46 +313,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int mt, nt;
             tile_coords(p, t, mt, nt);
             const int row0 = mt * C::kTileM + (int)rank * kRowsPerCta + quad * 32;
-            const int col0 = nt * kTileN;
-            const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kTileN;
+            const int col0 = nt * kBN;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
             if (row0 < p.M) {
-                for (int c = 0; c < kChunks; ++c) {
-                    const int ccol = col0 + c * kChunkCols;
-                    if (ccol >= p.N) break;
-                    uint32_t packed[32];
-                    if constexpr (kOut == kOutF32) {
-                        tmem_ld_32x32b_x32(t_row + c * kChunkCols, packed);
-                        tmem_ld_wait();
-                    } else {
-                        uint32_t lo[32], hi[32];
-                        tmem_ld_32x32b_x32(t_row + c * kChunkCols, lo);
-                        tmem_ld_32x32b_x32(t_row + c * kChunkCols + 32, hi);
-                        tmem_ld_wait();
+                // Two register sets: the TMEM load of chunk c+1 is in flight
+                // while chunk c is converted, staged and stored.
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(t_row, ra);
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            packed[q] = pack2(__uint_as_float(lo[2 * q]), __uint_as_float(lo[2 * q + 1]), kOut);
-                            packed[16 + q] = pack2(__uint_as_float(hi[2 * q]), __uint_as_float(hi[2 * q + 1]), kOut);
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                    uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                    if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
+                    const int ccol = col0 + c * kChunkCols;
+                    if (ccol < p.N) {
+                        const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
+                        ++slot;
+                        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
+                        __syncwarp();
+                        const uint32_t row_addr = buf + (uint32_t)lane * C::kRowBytes;
+                        if constexpr (kOut == kOutF32) {
+                            // 128-byte rows: 16-byte chunk q stored at q ^ (row % 8)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                st_shared_v4(row_addr + (((uint32_t)q ^ ((uint32_t)lane & 7u)) << 4), cur[4 * q],
+                                             cur[4 * q + 1], cur[4 * q + 2], cur[4 * q + 3]);
+                        } else {
+                            // 64-byte rows: 16-byte chunk q stored at q ^ ((row / 2) % 4)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t w0 = pack2(__uint_as_float(cur[8 * q + 0]), __uint_as_float(cur[8 * q + 1]), kOut);
+                                const uint32_t w1 = pack2(__uint_as_float(cur[8 * q + 2]), __uint_as_float(cur[8 * q + 3]), kOut);
+                                const uint32_t w2 = pack2(__uint_as_float(cur[8 * q + 4]), __uint_as_float(cur[8 * q + 5]), kOut);
+                                const uint32_t w3 = pack2(__uint_as_float(cur[8 * q + 6]), __uint_as_float(cur[8 * q + 7]), kOut);
+                                st_shared_v4(row_addr + (((uint32_t)q ^ (((uint32_t)lane >> 1) & 3u)) << 4), w0, w1, w2, w3);
+                            }
+                        }
+                        fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, buf, ccol, row0);
+                            bulk_commit_group();
                         }
                     }
-                    const uint32_t buf = staging + (slot & 1u) * kStagingSlotBytes;
-                    ++slot;
-                    if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
-                    __syncwarp();
-                    // Row `lane` of a 32×128-byte box, 16-byte chunk q stored at
-                    // chunk q ^ (row % 8): the 128-byte swizzle the TMA store undoes.
-                    const uint32_t row_addr = buf + (uint32_t)lane * 128u;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        st_shared_v4(row_addr + (((uint32_t)q ^ ((uint32_t)lane & 7u)) << 4), packed[4 * q],
-                                     packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                    }
-                    fence_proxy_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmC, buf, ccol, row0);
-                        bulk_commit_group();
-                    }
                 }
+                tmem_ld_wait();
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -370,13 +390,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc<kPair>(tmem_base, kTmemCols);
     }
-}
-
-// C = 0 for K == 0 (the empty sum).  `n16` 16-byte words.
-__global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16) {
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
-        c[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace gb300

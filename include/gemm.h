@@ -66,10 +66,12 @@ typedef struct gemm_plan* gemm_plan_t;
 /* Plan options (gemm_plan_set_option).  For tuning sweeps and tests; the
  * defaults are what the library picks itself. */
 typedef enum {
-    GEMM_OPT_CTA_PAIR = 1,       /* 2 (default): 2-CTA pairs, 256×256 tile per pair;
-                                    1: one CTA per 128×256 tile                         */
+    GEMM_OPT_CTA_PAIR = 1,       /* 2 (default): 2-CTA pairs, 256×BN tile per pair;
+                                    1: one CTA per 128×BN tile                          */
     GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
-    GEMM_OPT_MAX_CTAS = 3        /* cap on resident CTAs of the persistent grid (0 = all SMs) */
+    GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
+    GEMM_OPT_TILE_N = 4          /* tile width: 256, 224, 192, 160 or 128 (0 = chosen per
+                                    problem so the tile count fills whole waves)       */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan
@@ -107,6 +109,9 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status);
 
 /* Number of CTAs the last run on this plan launched (for reports). */
 int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
+
+/* Tile width BN the last run on this plan used (for reports). */
+int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);
 
 /* Free the plan.  The caller must have synchronised every stream that still
  * runs work of this plan.  gemm_run() then uses the newest remaining plan of

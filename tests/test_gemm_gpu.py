@@ -147,6 +147,46 @@ def test_persistent_loop_many_tiles(g, fresh_plan, pair, ctas, group):
         parity.assert_within(C, C_ref, S, out, f"pair={pair} ctas={ctas} group={group} out={out}")
 
 
+TILE_NS = [256, 224, 192, 160, 128]
+
+
+@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("tile_n", TILE_NS)
+def test_every_tile_width(g, fresh_plan, pair, tile_n):
+    """Each instantiated tile width, both pairings, all output types: ragged in
+    M, N and K, several tiles in each direction, few CTAs so each walks many
+    tiles; integer inputs bit-exact, random inputs within tolerance."""
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, tile_n)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, 4)
+    M, N, K = 600, 1000, 392
+    for out in OUTS:
+        A, B = draw(M, N, K, dist="int", seed=tile_n + out)
+        C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
+        assert g.gemm_plan_last_tile_n(fresh_plan) == tile_n
+        C_ref, _ = oracle_full(A, B)
+        want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(C, want), f"tile_n={tile_n} pair={pair} out={out}"
+        dtype = wl.F16 if out == wl.F16 else wl.BF16
+        A, B = draw(M, N, K, dtype=dtype, seed=tile_n * 3 + out)
+        C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
+        C_ref, S = oracle_full(A, B)
+        parity.assert_within(C, C_ref, S, out, f"tile_n={tile_n} pair={pair} out={out}")
+
+
+@pytest.mark.parametrize("name,expect", [("gemm_4096_bf16", 224), ("gemm_1024x4096x4096_f16", 224),
+                                         ("gemm_8192_bf16", 256)])
+def test_tile_width_choice_fills_waves(g, plan, name, expect):
+    """The host picks the width whose tile count fills whole waves of pairs."""
+    w = wl.WORKLOADS[name]
+    A = torch.zeros((w.M, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
+    B = torch.zeros((w.N, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
+    C = run(g, plan, A, B, w.out_dtype)
+    assert bool((C == 0).all())
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert g.gemm_plan_last_tile_n(plan) == expect
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16"]
