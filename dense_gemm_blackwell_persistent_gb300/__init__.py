@@ -27,9 +27,11 @@ GEMM_ERR_DRIVER = -5
 GEMM_ERR_NO_PLAN = -6
 GEMM_ERR_TIMEOUT = -7
 GEMM_ERR_NO_DEVICE = -8
-GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N = 1, 2, 3, 4
+GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N, GEMM_OPT_STREAM_K = 1, 2, 3, 4, 5
 
-LIB_PATH = _build.LIB
+# GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps).
+VARIANT = os.environ.get("GB300_GEMM_VARIANT", "")
+LIB_PATH = _build.lib_path(VARIANT)
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -52,11 +54,12 @@ _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_tile_n.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_destroy.argtypes = [_vp]
+_lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
-              "gemm_plan_destroy"):
+              "gemm_plan_trace", "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
 
 
@@ -127,6 +130,17 @@ def gemm_plan_last_tile_n(plan: int) -> int:
     n = _int(0)
     _check(_lib.gemm_plan_last_tile_n(_vp(plan), ctypes.byref(n)), "gemm_plan_last_tile_n")
     return n.value
+
+
+def gemm_plan_trace(plan: int):
+    """Timeline words of a GEMM_TRACE build as a [ctas, slots] uint64 array."""
+    import numpy as np
+    ctas, slots = _int(0), _int(0)
+    _lib.gemm_plan_trace(_vp(plan), None, 0, ctas, slots)
+    buf = np.zeros((ctas.value, slots.value), dtype=np.uint64)
+    _check(_lib.gemm_plan_trace(_vp(plan), buf.ctypes.data_as(_vp), buf.nbytes, ctypes.byref(ctas),
+                                ctypes.byref(slots)), "gemm_plan_trace")
+    return buf
 
 
 def gemm_plan_destroy(plan: int) -> None:

@@ -19,6 +19,15 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgb300gemm.so")
+# Build variants: "" is the product library; "trace" adds -DGEMM_TRACE
+# (per-CTA timeline stamps, read back with gemm_plan_trace).
+VARIANT_DEFINES = {"": [], "trace": ["-DGEMM_TRACE"]}
+
+
+def lib_path(variant: str = "") -> str:
+    if variant not in VARIANT_DEFINES:
+        raise ValueError(f"unknown library variant {variant!r}")
+    return LIB if not variant else os.path.join(LIBDIR, f"libgb300gemm_{variant}.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -40,10 +49,11 @@ def _sources():
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
@@ -59,17 +69,18 @@ def _compile(args):
     return res.stdout + res.stderr if verbose else ""
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
     """Compile every translation unit in parallel, then link the shared library."""
     from concurrent.futures import ThreadPoolExecutor
 
-    if not force and up_to_date():
-        return LIB
+    lib = lib_path(variant)
+    if not force and up_to_date(variant):
+        return lib
     os.makedirs(LIBDIR, exist_ok=True)
-    objdir = os.path.join(LIBDIR, f"obj{os.getpid()}")
+    objdir = os.path.join(LIBDIR, f"obj{variant}{os.getpid()}")
     os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
-    common = [nvcc, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c"]
+    common = [nvcc, *NVCC_FLAGS, *VARIANT_DEFINES[variant], "-I", INCLUDE, "-I", CSRC, "-c"]
     if verbose:
         common.insert(1, "-Xptxas=-v")
     jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose)]
@@ -82,15 +93,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
         logs = list(ex.map(_compile, jobs))
     if verbose:
         print("".join(logs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     objs = sorted(os.path.join(objdir, f) for f in os.listdir(objdir) if f.endswith(".o"))
     link = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     _compile((link, False))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     shutil.rmtree(objdir, ignore_errors=True)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                variant="trace" if "--trace" in sys.argv else ""))

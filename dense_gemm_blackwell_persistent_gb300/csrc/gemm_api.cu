@@ -103,7 +103,11 @@ struct gemm_plan {
     int pair = 2;
     int group_m = 0;
     int cap_ctas = 0;
-    int tile_n = 0;               // 0 = chosen per problem
+    int tile_n = 0;               // 0 = 256
+    int stream_k = 0;             // split the K work of a partial last wave (option)
+    float* d_partials = nullptr;  // stream-K workspace: 2 slots per unit
+    int* d_counters = nullptr;    // stream-K arrival counters
+    unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
     int* d_status = nullptr;      // 4 ints, see Params::status
     int last_grid = 0;
     int last_tile_n = 0;
@@ -138,27 +142,10 @@ int resident_units(const gemm_plan* plan, int pair) {
     return std::max(1, units);
 }
 
-// Tile width: the candidate that minimises (waves of resident units) ×
-// (width + a fixed per-tile cost of 32 columns), so that the tile count
-// fills whole waves; ties go to the wider tile.
-int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int pair) {
-    if (plan->tile_n > 0) return plan->tile_n;
-    const int64_t units = resident_units(plan, pair);
-    const int64_t tiles_m = (M + kRowsPerCta * pair - 1) / (kRowsPerCta * pair);
-    int best = kTileWidths[0];
-    int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < kNumTileWidths; ++i) {
-        const int bn = kTileWidths[i];
-        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
-        const int64_t waves = (tiles + units - 1) / units;
-        const int64_t cost = waves * (bn + 32);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = bn;
-        }
-    }
-    return best;
-}
+// Tile width.  One tcgen05.mma occupies the tensor pipe for about the same
+// time for every N from 128 to 256 (measured on GB300), so the full width of
+// 256 is the fast choice; narrower widths stay available as an option.
+int choose_tile_n(const gemm_plan* plan) { return plan->tile_n > 0 ? plan->tile_n : kTileWidths[0]; }
 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
            int out_dtype, cudaStream_t stream) {
@@ -169,7 +156,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
-    const int bn = choose_tile_n(plan, M, N, pair);
+    const int bn = choose_tile_n(plan);
     const KernelInfo ki = kernel_info(pair, bn, out_dtype);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * pair;
@@ -185,6 +172,15 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
     p.idesc = make_idesc(dtype, tile_m, bn);
     p.status = plan->d_status;
+    // Stream-K spreads a partial last wave over every resident unit; with
+    // whole tiles only, never launch more units than tiles.
+    const int resident = resident_units(plan, pair);
+    const bool sk = plan->stream_k && plan->d_partials != nullptr && plan->d_counters != nullptr;
+    p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
+    if (p.sched.sk_tiles == 0) p.sched = make_schedule(p.num_tiles, std::min(resident, p.num_tiles), p.k_blocks, false);
+    p.partials = plan->d_partials;
+    p.counters = plan->d_counters;
+    p.trace = plan->d_trace;
 
     CUtensorMap tmA, tmB, tmC;
     int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -199,7 +195,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc != GEMM_OK) return rc;
 
-    const int units = std::min(resident_units(plan, pair), p.num_tiles);
+    const int units = p.sched.units;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * pair), 1, 1);
@@ -221,6 +217,25 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     plan->last_grid = units * pair;
     plan->last_tile_n = bn;
     return GEMM_OK;
+}
+
+// Stream-K workspace: two partial slots per unit; a slot holds kPair CTAs ×
+// 4 epilogue warps × 32×256 fp32, i.e. 128 KB per CTA, for every CTA the
+// device can keep resident.
+size_t partials_bytes(const gemm_plan* plan) {
+    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    return (size_t)2 * ctas * 4 * kPartialFloats * sizeof(float);
+}
+// One counter per (tail tile, CTA of the pair, epilogue warp); a tail has
+// fewer tiles than units.
+size_t counters_bytes(const gemm_plan* plan) {
+    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    return (size_t)ctas * 2 * 4 * sizeof(int);
+}
+
+size_t trace_bytes(const gemm_plan* plan) {
+    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    return (size_t)ctas * kTraceSlots * sizeof(unsigned long long);
 }
 
 int query_capacity(gemm_plan* plan, int pair) {
@@ -289,8 +304,18 @@ int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
     if (rc == GEMM_OK) rc = query_capacity(plan, 2);
     if (rc == GEMM_OK && cudaMalloc(&plan->d_status, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMemset(plan->d_status, 0, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMalloc(&plan->d_partials, partials_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMalloc(&plan->d_counters, counters_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMemset(plan->d_counters, 0, counters_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+#ifdef GEMM_TRACE
+    if (rc == GEMM_OK && cudaMalloc(&plan->d_trace, trace_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMemset(plan->d_trace, 0, trace_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+#endif
     if (rc != GEMM_OK) {
+        cudaGetLastError();
         if (plan->d_status) cudaFree(plan->d_status);
+        if (plan->d_partials) cudaFree(plan->d_partials);
+        if (plan->d_counters) cudaFree(plan->d_counters);
         delete plan;
         cudaSetDevice(prev);
         return rc;
@@ -318,6 +343,10 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
         case GEMM_OPT_MAX_CTAS:
             if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
             plan->cap_ctas = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_STREAM_K:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            plan->stream_k = (int)value;
             return GEMM_OK;
         case GEMM_OPT_TILE_N: {
             if (value == 0) {
@@ -411,6 +440,12 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status) {
         return GEMM_ERR_CUDA;
     }
     *device_status = h[0];
+    // A run that gave up part-way may leave stream-K counters non-zero.
+    if (h[0] != 0 && plan->d_counters != nullptr &&
+        cudaMemset(plan->d_counters, 0, counters_bytes(plan)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     return GEMM_OK;
 }
 
@@ -423,6 +458,21 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
     if (!plan || !tile_n) return GEMM_ERR_INVALID_ARG;
     *tile_n = plan->last_tile_n;
+    return GEMM_OK;
+}
+
+int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* slots) {
+    if (!plan || !ctas || !slots) return GEMM_ERR_INVALID_ARG;
+    *ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    *slots = kTraceSlots;
+    if (plan->d_trace == nullptr) return GEMM_ERR_UNSUPPORTED;
+    const size_t need = trace_bytes(plan);
+    if (host == nullptr || bytes < need) return GEMM_ERR_INVALID_ARG;
+    if (cudaMemcpy(host, plan->d_trace, need, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(plan->d_trace, 0, need) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     return GEMM_OK;
 }
 
@@ -440,6 +490,9 @@ int gemm_plan_destroy(gemm_plan_t plan) {
     cudaGetDevice(&prev);
     cudaSetDevice(plan->device);
     if (plan->d_status) cudaFree(plan->d_status);
+    if (plan->d_partials) cudaFree(plan->d_partials);
+    if (plan->d_counters) cudaFree(plan->d_counters);
+    if (plan->d_trace) cudaFree(plan->d_trace);
     for (int i = 0; i < 3; ++i)
         if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);
     cudaSetDevice(prev);
@@ -526,6 +579,7 @@ void noalloc_setup(NoallocDevice* d, int device) {
     d->state.device = device;
     d->state.sm_count = prop.multiProcessorCount;
     d->state.d_status = static_cast<int*>(ptr);
+    d->state.stream_k = 0;   // no workspace here: whole tiles only
     int rc = query_capacity(&d->state, 1);
     if (rc == GEMM_OK) rc = query_capacity(&d->state, 2);
     d->rc = rc;

@@ -50,8 +50,34 @@
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace gb300 {
+
+// Optional timeline tracing (build with -DGEMM_TRACE): per-CTA
+// %globaltimer stamps and wait totals in a device buffer of kTraceSlots
+// 64-bit words per CTA.  Without GEMM_TRACE the macros compile to nothing.
+constexpr int kTraceSlots = 64;
+enum TraceSlot {
+    kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrFirstFull = 3, kTrTeardown = 4, kTrExit = 5,
+    kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8, kTrWorkItems = 9,
+    kTrMmaEnd = 16,       // + item (8 items)
+    kTrEpiStart = 24,     // + item
+    kTrEpiEnd = 32,       // + item
+    kTrPartialDone = 40,  // + item: stream-K partial published
+    kTrReduceDone = 48,   // + item: stream-K reduction finished (last contributor)
+};
+#ifdef GEMM_TRACE
+#define GEMM_TR(slot) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
+#define GEMM_TR_ITEM(base, item) do { if ((item) < 8) GEMM_TR((base) + (item)); } while (0)
+#define GEMM_TR_ADD(slot, v) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] += (v); } while (0)
+#define GEMM_TR_NOW() global_timer_ns()
+#else
+#define GEMM_TR(slot) do { } while (0)
+#define GEMM_TR_ITEM(base, item) do { } while (0)
+#define GEMM_TR_ADD(slot, v) do { } while (0)
+#define GEMM_TR_NOW() 0ull
+#endif
 
 constexpr int kNumThreads = 192;
 constexpr int kEpiWarps = 4;
@@ -71,8 +97,16 @@ struct Params {
     int M, N, K;
     int tiles_m, tiles_n, k_blocks, num_tiles, group_m;
     uint32_t idesc;
-    int* status;  // [0] first error code, [1] role, [2] block, [3] detail
+    int* status;       // [0] first error code, [1] role, [2] block, [3] detail
+    Schedule sched;    // data-parallel waves + stream-K tail
+    float* partials;   // stream-K partial tiles (2 slots per unit), or null
+    int* counters;     // stream-K arrival counters per (tail tile, CTA, quadrant)
+    unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
 };
+
+// fp32 partial of one epilogue warp: 32 rows × 256 columns, stored as
+// float4 groups [column/4][row] so that a warp's accesses are contiguous.
+constexpr int kPartialFloats = 32 * 256;
 
 // kPair: CTAs per tile (1 or 2); kBN: tile width (accumulator columns, a
 // multiple of 32 up to 256); kOut: C element type.
@@ -176,6 +210,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     constexpr int kChunks = kBN / kChunkCols;
 
     extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x == 0) GEMM_TR(kTrEntry);
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
@@ -191,7 +226,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kPair == 2 ? cluster_cta_rank() : 0u;
     const int pair_id = kPair == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
-    const int num_pairs = kPair == 2 ? (int)num_clusters_x() : (int)gridDim.x;
 
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
@@ -223,22 +257,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 0) GEMM_TR(kTrSetup);
 
     if (warp == 0) {
         // ================= TMA producer
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int t = pair_id; t < p.num_tiles && ok; t += num_pairs) {
+            const int nwork = work_count(p.sched, pair_id);
+            for (int j = 0; j < nwork && ok; ++j) {
+                const Work w = work_item(p.sched, pair_id, j);
                 int mt, nt;
-                tile_coords(p, t, mt, nt);
+                tile_coords(p, w.tile, mt, nt);
                 const int a_row = mt * C::kTileM + (int)rank * kRowsPerCta;
                 const int b_row = nt * kBN + (int)rank * C::kRowsB;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                    const uint64_t tw = GEMM_TR_NOW();
                     if (!wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
                         ok = false;
                         break;
                     }
+                    GEMM_TR_ADD(kTrEmptyWaitNs, GEMM_TR_NOW() - tw);
+                    if (j == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstLoad);
                     const uint32_t fb = full_bar(stage);
                     if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
                     const uint32_t a_dst = base + stage * kStageBytesA;
@@ -269,20 +309,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int i = 0;
-            for (int t = pair_id; t < p.num_tiles && ok; t += num_pairs, ++i) {
+            const int nwork = work_count(p.sched, pair_id);
+            for (; i < nwork && ok; ++i) {
+                const Work w = work_item(p.sched, pair_id, i);
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
+                const uint64_t ta = GEMM_TR_NOW();
                 if (!wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i)) { ok = false; break; }
+                GEMM_TR_ADD(kTrAccEmptyWaitNs, GEMM_TR_NOW() - ta);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                    const uint64_t tf = GEMM_TR_NOW();
                     if (!wait_bounded<false>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
+                    GEMM_TR_ADD(kTrFullWaitNs, GEMM_TR_NOW() - tf);
+                    if (i == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstFull);
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
                     const uint64_t bd = smem_desc_sw128(b_base + stage * C::kStageBytesB);
+                    const uint32_t first = kb == w.kb_begin;
 #pragma unroll
                     for (int j = 0; j < kBlockK / kMmaK; ++j) {
                         // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
-                        tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, (kb | j) != 0);
+                        tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
                     }
                     if constexpr (kPair == 2) tc_commit_pair(empty_bar(stage), 0x3);
                     else tc_commit(empty_bar(stage));
@@ -291,7 +339,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!ok) break;
                 if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), 0x3);
                 else tc_commit(accf_bar(b));
+                GEMM_TR_ITEM(kTrMmaEnd, i);
             }
+            GEMM_TR(kTrWorkItems);
             // Both accumulators must be released by every epilogue warp of the
             // pair (the peer's arrive on this CTA's barriers) before exit.
             for (int j = 0; j < 2 && ok; ++j, ++i) {
@@ -304,63 +354,139 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad+31
         const uint32_t staging = base + C::kOffStaging + (uint32_t)(warp - 2) * 2u * C::kSlotBytes;
         uint32_t slot = 0;
-        int i = 0;
-        for (int t = pair_id; t < p.num_tiles; t += num_pairs, ++i) {
+
+        // Convert one 32-column chunk (fp32 values of this thread's row),
+        // stage it swizzled and TMA-store it to C at (ccol, row0).
+        auto store_chunk = [&](const uint32_t (&cur)[32], int ccol, int row0) {
+            const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
+            ++slot;
+            if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
+            __syncwarp();
+            const uint32_t row_addr = buf + (uint32_t)lane * C::kRowBytes;
+            if constexpr (kOut == kOutF32) {
+                // 128-byte rows: 16-byte chunk q stored at q ^ (row % 8)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(row_addr + (((uint32_t)q ^ ((uint32_t)lane & 7u)) << 4), cur[4 * q], cur[4 * q + 1],
+                                 cur[4 * q + 2], cur[4 * q + 3]);
+            } else {
+                // 64-byte rows: 16-byte chunk q stored at q ^ ((row / 2) % 4)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t w0 = pack2(__uint_as_float(cur[8 * q + 0]), __uint_as_float(cur[8 * q + 1]), kOut);
+                    const uint32_t w1 = pack2(__uint_as_float(cur[8 * q + 2]), __uint_as_float(cur[8 * q + 3]), kOut);
+                    const uint32_t w2 = pack2(__uint_as_float(cur[8 * q + 4]), __uint_as_float(cur[8 * q + 5]), kOut);
+                    const uint32_t w3 = pack2(__uint_as_float(cur[8 * q + 6]), __uint_as_float(cur[8 * q + 7]), kOut);
+                    st_shared_v4(row_addr + (((uint32_t)q ^ (((uint32_t)lane >> 1) & 3u)) << 4), w0, w1, w2, w3);
+                }
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tmC, buf, ccol, row0);
+                bulk_commit_group();
+            }
+        };
+
+        const int nwork = work_count(p.sched, pair_id);
+        for (int i = 0; i < nwork; ++i) {
+            const Work w = work_item(p.sched, pair_id, i);
             const uint32_t b = i & 1, aphase = (i >> 1) & 1;
             const bool got = wait_bounded<false>(accf_bar(b), aphase, abort_flag, p, 5, i);
             if (!__all_sync(0xffffffffu, got)) break;
+            if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiStart, i);
             tc_fence_after_sync();
             int mt, nt;
-            tile_coords(p, t, mt, nt);
+            tile_coords(p, w.tile, mt, nt);
             const int row0 = mt * C::kTileM + (int)rank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
-            if (row0 < p.M) {
-                // Two register sets: the TMEM load of chunk c+1 is in flight
-                // while chunk c is converted, staged and stored.
-                uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(t_row, ra);
+            if (w.ncontrib == 1) {
+                if (row0 < p.M) {
+                    // Two register sets: the TMEM load of chunk c+1 is in flight
+                    // while chunk c is converted, staged and stored.
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(t_row, ra);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                        uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                        if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
+                        const int ccol = col0 + c * kChunkCols;
+                        if (ccol < p.N) store_chunk(cur, ccol, row0);
+                    }
+                    tmem_ld_wait();
+                }
+            } else {
+                // Stream-K segment: publish this partial, count the arrival,
+                // and let the last contributor of the tile finish it.
+                const size_t part_stride = (size_t)kPartialFloats;
+                float4* mine = reinterpret_cast<float4*>(
+                    p.partials + ((size_t)(w.slot * kPair + (int)rank) * 4 + quad) * part_stride);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
-                    uint32_t(&cur)[32] = (c & 1) ? rb : ra;
-                    uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
-                    if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
-                    const int ccol = col0 + c * kChunkCols;
-                    if (ccol < p.N) {
-                        const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
-                        ++slot;
-                        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
-                        __syncwarp();
-                        const uint32_t row_addr = buf + (uint32_t)lane * C::kRowBytes;
-                        if constexpr (kOut == kOutF32) {
-                            // 128-byte rows: 16-byte chunk q stored at q ^ (row % 8)
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + c * kChunkCols, v);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                st_shared_v4(row_addr + (((uint32_t)q ^ ((uint32_t)lane & 7u)) << 4), cur[4 * q],
-                                             cur[4 * q + 1], cur[4 * q + 2], cur[4 * q + 3]);
-                        } else {
-                            // 64-byte rows: 16-byte chunk q stored at q ^ ((row / 2) % 4)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const uint32_t w0 = pack2(__uint_as_float(cur[8 * q + 0]), __uint_as_float(cur[8 * q + 1]), kOut);
-                                const uint32_t w1 = pack2(__uint_as_float(cur[8 * q + 2]), __uint_as_float(cur[8 * q + 3]), kOut);
-                                const uint32_t w2 = pack2(__uint_as_float(cur[8 * q + 4]), __uint_as_float(cur[8 * q + 5]), kOut);
-                                const uint32_t w3 = pack2(__uint_as_float(cur[8 * q + 6]), __uint_as_float(cur[8 * q + 7]), kOut);
-                                st_shared_v4(row_addr + (((uint32_t)q ^ (((uint32_t)lane >> 1) & 3u)) << 4), w0, w1, w2, w3);
-                            }
-                        }
-                        fence_proxy_async_shared();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, buf, ccol, row0);
-                            bulk_commit_group();
-                        }
-                    }
+                    for (int q = 0; q < 8; ++q)
+                        __stcg(&mine[(c * 8 + q) * 32 + lane],
+                               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                 }
                 tmem_ld_wait();
+                __threadfence();
+                __syncwarp();
+                if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrPartialDone, i);
+                int* counter = p.counters + (w.sk_index * 2 + (int)rank) * 4 + quad;
+                int prev = 0;
+                if (lane == 0) prev = atomicAdd(counter, 1);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == w.ncontrib - 1) {
+                    __threadfence();
+                    if (row0 < p.M) {
+#pragma unroll 1
+                        for (int c = 0; c < kChunks; ++c) {
+                            const int ccol = col0 + c * kChunkCols;
+                            if (ccol >= p.N) break;
+                            uint32_t own[32];
+                            tmem_ld_32x32b_x32(t_row + c * kChunkCols, own);
+                            tmem_ld_wait();
+                            float acc[32];
+                            for (int k = 0; k < w.ncontrib; ++k) {   // contributor order: fixed sum order
+                                float part[32];
+                                if (k == w.contrib) {
+#pragma unroll
+                                    for (int e = 0; e < 32; ++e) part[e] = __uint_as_float(own[e]);
+                                } else {
+                                    const float4* src = reinterpret_cast<const float4*>(
+                                        p.partials +
+                                        ((size_t)(contributor_slot(p.sched, w.sk_index, k) * kPair + (int)rank) * 4 +
+                                         quad) * part_stride);
+#pragma unroll
+                                    for (int q = 0; q < 8; ++q) {
+                                        const float4 f = __ldcg(&src[(c * 8 + q) * 32 + lane]);
+                                        part[4 * q] = f.x;
+                                        part[4 * q + 1] = f.y;
+                                        part[4 * q + 2] = f.z;
+                                        part[4 * q + 3] = f.w;
+                                    }
+                                }
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) acc[e] = k == 0 ? part[e] : acc[e] + part[e];
+                            }
+                            uint32_t sum[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) sum[e] = __float_as_uint(acc[e]);
+                            store_chunk(sum, ccol, row0);
+                        }
+                    }
+                    if (lane == 0) *counter = 0;   // ready for the next launch
+                    if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrReduceDone, i);
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
+            if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiEnd, i);
             if (lane == 0) {
                 if constexpr (kPair == 2) mbar_arrive_cluster(map_shared_rank(acce_bar(b), 0));
                 else mbar_arrive_local(acce_bar(b));
@@ -373,6 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ---- teardown
     tc_fence_before_sync();
     __syncthreads();
+    if (threadIdx.x == 0) GEMM_TR(kTrTeardown);
     if (*abort_flag) {
         // A bounded wait gave up: let copies and MMAs already in flight land
         // (they finish in microseconds) before TMEM and shared memory go away.
@@ -390,6 +517,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc<kPair>(tmem_base, kTmemCols);
     }
+    if (threadIdx.x == 0) GEMM_TR(kTrExit);
 }
 
 }  // namespace gb300

@@ -1,0 +1,104 @@
+"""Timeline of one persistent-GEMM launch from a GEMM_TRACE build.
+
+    python -c "from dense_gemm_blackwell_persistent_gb300 import _build; _build.build(variant='trace')"
+    GB300_GEMM_VARIANT=trace python -m dense_gemm_blackwell_persistent_gb300.timeline --M 4096 --N 4096 --K 4096
+
+Runs a few warm-up launches, clears the trace, runs one launch and prints,
+for every trace point, the earliest / median / latest time over the CTAs
+(µs from the first CTA's entry) and the per-CTA wait totals.  --json writes
+the same summary to a file.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+import torch
+
+from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_STREAM_K, GEMM_OPT_TILE_N, VARIANT,
+               gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_run,
+               gemm_plan_set_option, gemm_plan_trace)
+
+POINTS = {0: "entry", 1: "setup_done", 2: "first_load_issued", 3: "first_full", 4: "teardown", 5: "exit"}
+ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published", 48: "reduce_done"}
+TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us"}
+
+
+def summarise(buf: np.ndarray, ctas: int) -> dict:
+    t = buf[:ctas].astype(np.int64)
+    t0 = t[:, 0][t[:, 0] > 0].min()
+    out = {}
+
+    def stats(col):
+        v = t[:, col]
+        v = v[v > 0]
+        if v.size == 0:
+            return None
+        r = (v - t0) / 1e3
+        return [round(float(r.min()), 2), round(float(np.median(r)), 2), round(float(r.max()), 2), int(v.size)]
+
+    for col, name in POINTS.items():
+        s = stats(col)
+        if s:
+            out[name] = s
+    for base, name in ITEMS.items():
+        for j in range(8):
+            s = stats(base + j)
+            if s:
+                out[f"{name}[{j}]"] = s
+    for col, name in TOTALS.items():
+        v = t[:, col][t[:, col] > 0] / 1e3
+        if v.size:
+            out[name] = [round(float(v.min()), 2), round(float(np.median(v)), 2), round(float(v.max()), 2),
+                         int(v.size)]
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--M", type=int, default=4096)
+    ap.add_argument("--N", type=int, default=4096)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--dtype", type=int, default=0, help="0 bf16, 1 f16")
+    ap.add_argument("--out", type=int, default=0, help="0 bf16, 1 f16, 2 fp32")
+    ap.add_argument("--pair", type=int, default=2)
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--stream-k", type=int, default=1)
+    ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--json", default="")
+    a = ap.parse_args()
+    if VARIANT != "trace":
+        raise SystemExit("set GB300_GEMM_VARIANT=trace (and build that variant) to record a timeline")
+    torch.cuda.set_device(0)
+    plan = gemm_plan_create(0)
+    gemm_plan_set_option(plan, GEMM_OPT_CTA_PAIR, a.pair)
+    gemm_plan_set_option(plan, GEMM_OPT_TILE_N, a.tile_n)
+    gemm_plan_set_option(plan, GEMM_OPT_STREAM_K, a.stream_k)
+    gemm_plan_set_option(plan, GEMM_OPT_MAX_CTAS, a.max_ctas)
+    tin = torch.bfloat16 if a.dtype == 0 else torch.float16
+    tout = {0: torch.bfloat16, 1: torch.float16, 2: torch.float32}[a.out]
+    A = torch.randn(a.M, a.K, device="cuda").to(tin)
+    B = torch.randn(a.N, a.K, device="cuda").to(tin)
+    C = torch.empty(a.M, a.N, device="cuda", dtype=tout)
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), a.M, a.N, a.K, a.dtype, a.out, s)
+    torch.cuda.synchronize()
+    gemm_plan_trace(plan)
+    gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), a.M, a.N, a.K, a.dtype, a.out, s)
+    torch.cuda.synchronize()
+    buf = gemm_plan_trace(plan)
+    res = summarise(buf, gemm_plan_last_grid(plan))
+    print(f"{a.M}x{a.N}x{a.K} pair={a.pair} tile_n={a.tile_n or 256} stream_k={a.stream_k}: "
+          "[earliest, median, latest] µs over CTAs, count")
+    for k, v in res.items():
+        print(f"  {k:26s} {v}")
+    if a.json:
+        with open(a.json, "w") as f:
+            json.dump(res, f, indent=1)
+    gemm_plan_destroy(plan)
+
+
+if __name__ == "__main__":
+    main()

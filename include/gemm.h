@@ -41,6 +41,7 @@
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -70,15 +71,19 @@ typedef enum {
                                     1: one CTA per 128×BN tile                          */
     GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
-    GEMM_OPT_TILE_N = 4          /* tile width: 256, 224, 192, 160 or 128 (0 = chosen per
-                                    problem so the tile count fills whole waves)       */
+    GEMM_OPT_TILE_N = 4,         /* tile width: 256 (default, also 0), 224, 192, 160 or 128 */
+    GEMM_OPT_STREAM_K = 5        /* 1: spread the K work of a partial last wave over all
+                                    resident CTA pairs (stream-K tail, deterministic
+                                    fixup); 0 (default): whole tiles only              */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan
- * gemm_run() uses on that device while it is the newest one alive.  Queries the SM count and the resident
- * cluster capacity, sets kernel attributes and allocates one 4-byte device
- * status word (the only device memory the library owns).  `flags` must be 0.
- * The caller owns the plan and frees it with gemm_plan_destroy(). */
+ * gemm_run() uses on that device while it is the newest one alive.  Queries
+ * the SM count and the resident cluster capacity, sets kernel attributes and
+ * allocates the plan's device memory: a 16-byte status record and the
+ * stream-K workspace (256 KB of fp32 partials per SM, about 40 MB on GB300,
+ * plus a few KB of counters).  `flags` must be 0.  The caller owns the plan
+ * and frees it with gemm_plan_destroy(). */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
 
 /* Set a plan option (see gemm_option_t).  Not thread-safe with concurrent
@@ -104,7 +109,8 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
 
 /* Read and clear the plan's device status word.  Synchronises the device.
  * *device_status receives GEMM_OK or the first device-side error code
- * recorded since the last call. */
+ * recorded since the last call; after an error the stream-K counters are
+ * reset too, so the plan can be used again. */
 int gemm_plan_status(gemm_plan_t plan, int* device_status);
 
 /* Number of CTAs the last run on this plan launched (for reports). */
@@ -112,6 +118,14 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
 
 /* Tile width BN the last run on this plan used (for reports). */
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);
+
+/* Timeline of the last runs, for builds compiled with GEMM_TRACE (other
+ * builds return GEMM_ERR_UNSUPPORTED after filling *ctas and *slots).  Copies
+ * *ctas × *slots 64-bit words to `host` (at least that many bytes) and
+ * clears the device buffer; synchronises the device.  Word s of CTA c is a
+ * %globaltimer stamp in ns (or a wait total) at trace point s; see
+ * TraceSlot in the kernel source. */
+int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* slots);
 
 /* Free the plan.  The caller must have synchronised every stream that still
  * runs work of this plan.  gemm_run() then uses the newest remaining plan of

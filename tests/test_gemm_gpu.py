@@ -150,6 +150,7 @@ def test_persistent_loop_many_tiles(g, fresh_plan, pair, ctas, group):
 TILE_NS = [256, 224, 192, 160, 128]
 
 
+
 @pytest.mark.parametrize("pair", [2, 1])
 @pytest.mark.parametrize("tile_n", TILE_NS)
 def test_every_tile_width(g, fresh_plan, pair, tile_n):
@@ -174,17 +175,61 @@ def test_every_tile_width(g, fresh_plan, pair, tile_n):
         parity.assert_within(C, C_ref, S, out, f"tile_n={tile_n} pair={pair} out={out}")
 
 
-@pytest.mark.parametrize("name,expect", [("gemm_4096_bf16", 224), ("gemm_1024x4096x4096_f16", 224),
-                                         ("gemm_8192_bf16", 256)])
-def test_tile_width_choice_fills_waves(g, plan, name, expect):
-    """The host picks the width whose tile count fills whole waves of pairs."""
-    w = wl.WORKLOADS[name]
+def test_default_tile_width_is_full(g, plan):
+    """Every tcgen05.mma occupies the tensor pipe about equally long for N in
+    128..256, so the default tile is the full 256 columns."""
+    w = wl.WORKLOADS["gemm_4096_bf16"]
     A = torch.zeros((w.M, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
     B = torch.zeros((w.N, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
     C = run(g, plan, A, B, w.out_dtype)
     assert bool((C == 0).all())
-    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert g.gemm_plan_last_tile_n(plan) == expect
+    assert g.gemm_plan_last_tile_n(plan) == 256
+
+
+# (M, N, K, max CTAs): shapes whose last wave is split along K over all units
+STREAM_K_CASES = [
+    (1024, 1280, 1024, 0),   # 20 tiles over every resident pair: ~4 contributors per tile
+    (700, 1000, 1000, 10),   # 12 tiles on 5 pairs: 2 full waves + 2 split tiles
+    (520, 776, 2056, 6),     # 3 pairs, ragged M/N/K
+]
+
+
+@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("case", STREAM_K_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_stream_k_tail(g, fresh_plan, pair, case):
+    M, N, K, ctas = case
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, ctas)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STREAM_K, 1)
+    for out in OUTS:
+        # integer inputs: exact whatever the split
+        A, B = draw(M, N, K, dist="int", seed=K + out)
+        C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
+        C_ref, _ = oracle_full(A, B)
+        want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(C, want), f"stream-K {case} pair={pair} out={out}"
+        # random inputs: tolerance, and bitwise repeatable (fixed reduction order)
+        dtype = wl.F16 if out == wl.F16 else wl.BF16
+        A, B = draw(M, N, K, dtype=dtype, seed=K * 7 + out)
+        Ad, Bd = A.cuda(), B.cuda()
+        C1 = run(g, fresh_plan, Ad, Bd, out)
+        C2 = run(g, fresh_plan, Ad, Bd, out)
+        assert torch.equal(C1.view(torch.uint8), C2.view(torch.uint8)), "stream-K result not repeatable"
+        C_ref, S = oracle_full(A, B)
+        parity.assert_within(parity.to_f64(C1), C_ref, S, out, f"stream-K {case} pair={pair} out={out}")
+
+
+def test_stream_k_off_matches_within_tolerance(g, fresh_plan):
+    M, N, K = 1024, 1280, 1024
+    A, B = draw(M, N, K, seed=77)
+    Ad, Bd = A.cuda(), B.cuda()
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STREAM_K, 1)
+    C_on = parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32))
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STREAM_K, 0)
+    C_off = parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32))
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(C_on, C_ref, S, wl.F32, "stream-K on")
+    parity.assert_within(C_off, C_ref, S, wl.F32, "stream-K off")
 
 
 # ------------------------------------------------------------------ full-size workloads
