@@ -28,6 +28,7 @@ GEMM_ERR_NO_PLAN = -6
 GEMM_ERR_TIMEOUT = -7
 GEMM_ERR_NO_DEVICE = -8
 GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N, GEMM_OPT_STREAM_K = 1, 2, 3, 4, 5
+GEMM_OPT_MULTICAST = 6
 
 # GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps).
 VARIANT = os.environ.get("GB300_GEMM_VARIANT", "")
@@ -53,12 +54,14 @@ _lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_tile_n.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.gemm_plan_last_launch.argtypes = [_vp] + [ctypes.POINTER(_int)] * 5
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
+              "gemm_plan_last_launch",
               "gemm_plan_trace", "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
 
@@ -130,6 +133,13 @@ def gemm_plan_last_tile_n(plan: int) -> int:
     n = _int(0)
     _check(_lib.gemm_plan_last_tile_n(_vp(plan), ctypes.byref(n)), "gemm_plan_last_tile_n")
     return n.value
+
+
+def gemm_plan_last_launch(plan: int) -> dict:
+    v = [_int(0) for _ in range(5)]
+    _check(_lib.gemm_plan_last_launch(_vp(plan), *[ctypes.byref(x) for x in v]), "gemm_plan_last_launch")
+    keys = ("ctas", "ctas_per_unit", "tile_n", "dp_waves", "sk_tiles")
+    return {k: x.value for k, x in zip(keys, v)}
 
 
 def gemm_plan_trace(plan: int):

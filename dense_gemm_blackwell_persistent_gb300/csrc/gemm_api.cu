@@ -99,8 +99,9 @@ __global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16) {
 struct gemm_plan {
     int device = 0;
     int sm_count = 0;
-    int max_ctas[3] = {0, 0, 0};  // resident CTAs for pair = 1, 2 (index by pair)
-    int pair = 2;
+    int max_ctas[5] = {0, 0, 0, 0, 0};  // resident CTAs per unit size 1, 2, 4 (index by size)
+    int pair = 2;                 // CTAs per MMA
+    int multicast = -1;           // with pairs: share B across two pairs (1), never (0), auto (-1)
     int group_m = 0;
     int cap_ctas = 0;
     int tile_n = 0;               // 0 = 256
@@ -111,6 +112,9 @@ struct gemm_plan {
     int* d_status = nullptr;      // 4 ints, see Params::status
     int last_grid = 0;
     int last_tile_n = 0;
+    int last_unit = 0;
+    int last_dp_waves = 0;
+    int last_sk_tiles = 0;
     std::mutex host_mu;           // serialises gemm_plan_run_host's buffers
     void* hbuf[3] = {nullptr, nullptr, nullptr};
     size_t hcap[3] = {0, 0, 0};
@@ -135,10 +139,22 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     return GEMM_OK;
 }
 
-// Resident CTA pairs (units) a launch may use.
-int resident_units(const gemm_plan* plan, int pair) {
-    int units = plan->max_ctas[pair] / pair;
-    if (plan->cap_ctas > 0) units = std::min(units, std::max(1, plan->cap_ctas / pair));
+// CTAs per work unit: 1 (single CTA), 2 (a CTA pair) or 4 (two pairs
+// sharing B through TMA multicast).  Automatic choice: when the operand rows
+// are not a multiple of 128 bytes every 128-byte box row straddles an extra
+// 32-byte sector, the load path becomes the bound, and halving the B reads
+// wins (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of
+// all SMs wins (4-CTA clusters fit on 144 of the 152 SMs).
+int unit_ctas(const gemm_plan* plan, int64_t K) {
+    if (plan->pair != 2) return 1;
+    const bool mc = plan->multicast == 1 || (plan->multicast < 0 && (K * 2) % 128 != 0);
+    return mc ? 4 : 2;
+}
+
+// Resident units a launch may use.
+int resident_units(const gemm_plan* plan, int cluster) {
+    int units = plan->max_ctas[cluster] / cluster;
+    if (plan->cap_ctas > 0) units = std::min(units, std::max(1, plan->cap_ctas / cluster));
     return std::max(1, units);
 }
 
@@ -156,10 +172,11 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
+    const int cluster = unit_ctas(plan, K);
     const int bn = choose_tile_n(plan);
-    const KernelInfo ki = kernel_info(pair, bn, out_dtype);
+    const KernelInfo ki = kernel_info(cluster, bn, out_dtype);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
-    const int tile_m = kRowsPerCta * pair;
+    const int tile_m = kRowsPerCta * cluster;
     Params p;
     p.M = (int)M;
     p.N = (int)N;
@@ -170,11 +187,11 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
-    p.idesc = make_idesc(dtype, tile_m, bn);
+    p.idesc = make_idesc(dtype, kRowsPerCta * pair, bn);   // one MMA covers a pair's 256 rows
     p.status = plan->d_status;
     // Stream-K spreads a partial last wave over every resident unit; with
     // whole tiles only, never launch more units than tiles.
-    const int resident = resident_units(plan, pair);
+    const int resident = resident_units(plan, cluster);
     const bool sk = plan->stream_k && plan->d_partials != nullptr && plan->d_counters != nullptr;
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
     if (p.sched.sk_tiles == 0) p.sched = make_schedule(p.num_tiles, std::min(resident, p.num_tiles), p.k_blocks, false);
@@ -186,7 +203,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / pair), kBlockK,
+        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), kBlockK,
                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
@@ -198,13 +215,13 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     const int units = p.sched.units;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * pair), 1, 1);
+    cfg.gridDim = dim3((unsigned)(units * cluster), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)ki.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pair;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -214,36 +231,43 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    plan->last_grid = units * pair;
+    plan->last_grid = units * cluster;
     plan->last_tile_n = bn;
+    plan->last_unit = cluster;
+    plan->last_dp_waves = p.sched.dp_waves;
+    plan->last_sk_tiles = p.sched.sk_tiles;
     return GEMM_OK;
 }
 
 // Stream-K workspace: two partial slots per unit; a slot holds kPair CTAs ×
 // 4 epilogue warps × 32×256 fp32, i.e. 128 KB per CTA, for every CTA the
 // device can keep resident.
+int max_resident_ctas(const gemm_plan* plan) {
+    return std::max(plan->max_ctas[1], std::max(plan->max_ctas[2], plan->max_ctas[4]));
+}
+
 size_t partials_bytes(const gemm_plan* plan) {
-    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    const int ctas = max_resident_ctas(plan);
     return (size_t)2 * ctas * 4 * kPartialFloats * sizeof(float);
 }
 // One counter per (tail tile, CTA of the pair, epilogue warp); a tail has
 // fewer tiles than units.
 size_t counters_bytes(const gemm_plan* plan) {
-    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    const int ctas = max_resident_ctas(plan);
     return (size_t)ctas * 2 * 4 * sizeof(int);
 }
 
 size_t trace_bytes(const gemm_plan* plan) {
-    const int ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    const int ctas = max_resident_ctas(plan);
     return (size_t)ctas * kTraceSlots * sizeof(unsigned long long);
 }
 
-int query_capacity(gemm_plan* plan, int pair) {
+int query_capacity(gemm_plan* plan, int cluster) {
     int max_smem = 0;
     KernelFn probe = nullptr;
     for (int out = 0; out < 3; ++out) {
         for (int i = 0; i < kNumTileWidths; ++i) {
-            const KernelInfo ki = kernel_info(pair, kTileWidths[i], out);
+            const KernelInfo ki = kernel_info(cluster, kTileWidths[i], out);
             if (ki.fn == nullptr) continue;
             if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem_bytes) !=
                 cudaSuccess) {
@@ -257,12 +281,12 @@ int query_capacity(gemm_plan* plan, int pair) {
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(plan->sm_count / pair * pair), 1, 1);
+    cfg.gridDim = dim3((unsigned)(plan->sm_count / cluster * cluster), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)max_smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pair;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -270,9 +294,9 @@ int query_capacity(gemm_plan* plan, int pair) {
     int clusters = 0;
     if (probe == nullptr || cudaOccupancyMaxActiveClusters(&clusters, probe, &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
-        clusters = plan->sm_count / pair;  // one CTA per SM is what the shared-memory budget allows
+        clusters = plan->sm_count / cluster;  // one CTA per SM is what the shared-memory budget allows
     }
-    plan->max_ctas[pair] = clusters * pair;
+    plan->max_ctas[cluster] = clusters * cluster;
     return GEMM_OK;
 }
 
@@ -302,6 +326,7 @@ int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
     plan->sm_count = prop.multiProcessorCount;
     int rc = query_capacity(plan, 1);
     if (rc == GEMM_OK) rc = query_capacity(plan, 2);
+    if (rc == GEMM_OK) rc = query_capacity(plan, 4);
     if (rc == GEMM_OK && cudaMalloc(&plan->d_status, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMemset(plan->d_status, 0, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMalloc(&plan->d_partials, partials_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
@@ -343,6 +368,10 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
         case GEMM_OPT_MAX_CTAS:
             if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
             plan->cap_ctas = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_MULTICAST:
+            if (value < -1 || value > 1) return GEMM_ERR_INVALID_ARG;
+            plan->multicast = (int)value;
             return GEMM_OK;
         case GEMM_OPT_STREAM_K:
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
@@ -455,6 +484,17 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
     return GEMM_OK;
 }
 
+int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* tile_n, int* dp_waves,
+                          int* sk_tiles) {
+    if (!plan || !ctas || !ctas_per_unit || !tile_n || !dp_waves || !sk_tiles) return GEMM_ERR_INVALID_ARG;
+    *ctas = plan->last_grid;
+    *ctas_per_unit = plan->last_unit;
+    *tile_n = plan->last_tile_n;
+    *dp_waves = plan->last_dp_waves;
+    *sk_tiles = plan->last_sk_tiles;
+    return GEMM_OK;
+}
+
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
     if (!plan || !tile_n) return GEMM_ERR_INVALID_ARG;
     *tile_n = plan->last_tile_n;
@@ -463,7 +503,7 @@ int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
 
 int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* slots) {
     if (!plan || !ctas || !slots) return GEMM_ERR_INVALID_ARG;
-    *ctas = std::max(plan->max_ctas[1], plan->max_ctas[2]);
+    *ctas = max_resident_ctas(plan);
     *slots = kTraceSlots;
     if (plan->d_trace == nullptr) return GEMM_ERR_UNSUPPORTED;
     const size_t need = trace_bytes(plan);
@@ -582,6 +622,7 @@ void noalloc_setup(NoallocDevice* d, int device) {
     d->state.stream_k = 0;   // no workspace here: whole tiles only
     int rc = query_capacity(&d->state, 1);
     if (rc == GEMM_OK) rc = query_capacity(&d->state, 2);
+    if (rc == GEMM_OK) rc = query_capacity(&d->state, 4);
     d->rc = rc;
 }
 

@@ -20,12 +20,17 @@
 // The tile width kBN (256, 224, 192, 160 or 128) is chosen per problem on
 // the host so that the tile count fills whole waves of resident CTA pairs.
 //
-// With kPair == 2 two CTAs of a cluster form one 256×kBN tile: each holds its
-// own 128 rows of A and kBN/2 rows (half) of B, the leader issues
+// With a CTA pair (kCluster >= 2) two CTAs form one 256×kBN tile: each holds
+// its own 128 rows of A and kBN/2 rows (half) of B, the leader issues
 // tcgen05.mma.cta_group::2 with M = 256, and each CTA's TMEM receives its own
 // 128 rows of the result.  This is the collective MMA of "Writing Mosaic GPU
 // kernels with Pallas", "Collective MMA" (A and D per CTA, B split between
 // the pair) with the B halves loaded as partitioned, leader-tracked copies.
+// With kCluster == 4 two such pairs stacked along M share their B tile: the
+// same-rank CTAs of the two pairs each fetch half of their common B rows and
+// multicast it to both ("Writing Mosaic GPU kernels with Pallas", clusters
+// and collective copies: every CTA on the cluster axis issues the identical
+// copy and receives the data), which cuts L2-to-SM traffic by a quarter.
 //
 // Design sources on the pages (prior art, restated for this hardware):
 //   * tiles of A (BM×BK) and B (BN×BK) staged in shared memory, loaded by
@@ -70,12 +75,12 @@ enum TraceSlot {
 #ifdef GEMM_TRACE
 #define GEMM_TR(slot) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
 #define GEMM_TR_ITEM(base, item) do { if ((item) < 8) GEMM_TR((base) + (item)); } while (0)
-#define GEMM_TR_ADD(slot, v) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] += (v); } while (0)
+#define GEMM_TR_SET(slot, v) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = (v); } while (0)
 #define GEMM_TR_NOW() global_timer_ns()
 #else
 #define GEMM_TR(slot) do { } while (0)
 #define GEMM_TR_ITEM(base, item) do { } while (0)
-#define GEMM_TR_ADD(slot, v) do { } while (0)
+#define GEMM_TR_SET(slot, v) do { } while (0)
 #define GEMM_TR_NOW() 0ull
 #endif
 
@@ -108,16 +113,23 @@ struct Params {
 // float4 groups [column/4][row] so that a warp's accesses are contiguous.
 constexpr int kPartialFloats = 32 * 256;
 
-// kPair: CTAs per tile (1 or 2); kBN: tile width (accumulator columns, a
-// multiple of 32 up to 256); kOut: C element type.
-template <int kPair, int kBN, int kOut>
+// kCluster: CTAs per work unit -- 1 (one CTA, tcgen05 cta_group::1), 2 (a
+// CTA pair issuing cta_group::2 MMAs) or 4 (two pairs stacked along M that
+// share the B tile: each CTA loads a quarter of it and multicasts it to
+// the same-rank CTA of the other pair).  kBN: tile width (accumulator
+// columns, a multiple of 32 up to 256).  kOut: C element type.
+template <int kCluster, int kBN, int kOut>
 struct Cfg {
-    static_assert(kPair == 1 || kPair == 2, "one CTA or a CTA pair per tile");
+    static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "1, 2 or 4 CTAs per unit");
     static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "tile width");
-    static_assert((kBN / kPair) % 8 == 0, "B rows per CTA must fill 1 KB swizzle atoms");
-    static constexpr int kTileM = kRowsPerCta * kPair;          // rows per (pair) tile
-    static constexpr int kRowsB = kBN / kPair;                  // B rows held per CTA
+    static constexpr int kPair = kCluster >= 2 ? 2 : 1;           // CTAs per MMA
+    static constexpr int kPairs = kCluster / kPair;                // MMA groups per unit
+    static constexpr int kTileM = kRowsPerCta * kCluster;         // rows per unit tile
+    static constexpr int kRowsB = kBN / kPair;                    // B rows held per CTA
+    static constexpr int kRowsBLoad = kBN / kCluster;             // B rows each CTA loads
+    static_assert(kRowsBLoad % 8 == 0, "B boxes must fill 1 KB swizzle atoms");
     static constexpr int kStageBytesB = kRowsB * kBlockK * 2;
+    static constexpr int kLoadBytesB = kRowsBLoad * kBlockK * 2;
     static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
     static constexpr int kOutBytes = kOut == kOutF32 ? 4 : 2;
     static constexpr int kRowBytes = kChunkCols * kOutBytes;    // 128 (fp32) or 64 (16-bit)
@@ -136,7 +148,7 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert((2 * kStages + 4) * 8 <= kBarBytes, "barrier area");
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
-    static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // both CTAs' copies land on the leader
+    static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // bytes landing in a pair, tracked by its leader
 };
 
 // tcgen05 shared-memory matrix descriptor for a K-major tile written by TMA
@@ -201,11 +213,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
     }
 }
 
-template <int kPair, int kBN, int kOut>
+template <int kCluster, int kBN, int kOut>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tn_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const Params p) {
-    using C = Cfg<kPair, kBN, kOut>;
+    using C = Cfg<kCluster, kBN, kOut>;
+    constexpr int kPair = C::kPair;
     constexpr int kStages = C::kStages;
     constexpr int kChunks = kBN / kChunkCols;
 
@@ -224,14 +237,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = kPair == 2 ? cluster_cta_rank() : 0u;
-    const int pair_id = kPair == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
+    const uint32_t crank = kCluster > 1 ? cluster_cta_rank() : 0u;   // rank in the unit's cluster
+    const uint32_t rank = crank & (uint32_t)(kPair - 1);             // rank in the MMA pair (0 = leader)
+    const uint32_t pidx = crank / kPair;                             // which pair of the unit
+    const uint32_t leader = crank & ~(uint32_t)(kPair - 1);          // cluster rank of this pair's leader
+    const int pair_id = kCluster > 1 ? (int)cluster_id_x() : (int)blockIdx.x;   // work unit
 
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), C::kPairs);   // one MMA commit per pair that reads this slot
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kPair == 2) {
+    if constexpr (kCluster > 1) {
         cluster_arrive();
         cluster_wait();
     }
@@ -264,27 +280,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            uint64_t empty_wait_ns = 0;   // trace builds only
             const int nwork = work_count(p.sched, pair_id);
             for (int j = 0; j < nwork && ok; ++j) {
                 const Work w = work_item(p.sched, pair_id, j);
                 int mt, nt;
                 tile_coords(p, w.tile, mt, nt);
-                const int a_row = mt * C::kTileM + (int)rank * kRowsPerCta;
-                const int b_row = nt * kBN + (int)rank * C::kRowsB;
+                const int a_row = mt * C::kTileM + (int)crank * kRowsPerCta;
+                const int b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tw = GEMM_TR_NOW();
-                    if (!wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
+                    if (!wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
                         ok = false;
                         break;
                     }
-                    GEMM_TR_ADD(kTrEmptyWaitNs, GEMM_TR_NOW() - tw);
+                    empty_wait_ns += GEMM_TR_NOW() - tw;
                     if (j == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstLoad);
                     const uint32_t fb = full_bar(stage);
                     if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
                     const uint32_t a_dst = base + stage * kStageBytesA;
                     const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
-                    if constexpr (kPair == 2) {
-                        const uint32_t fb_leader = map_shared_rank(fb, 0);
+                    if constexpr (kCluster == 4) {
+                        // own A rows; a quarter of the pair-tile's B rows, written to
+                        // this CTA and to the same-rank CTA of the other pair
+                        const uint32_t fb_leader = map_shared_rank(fb, leader);
+                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                        tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
+                        tma_load_2d_pair_multicast(b_dst + pidx * C::kLoadBytesB, &tmB, fb_leader, mask,
+                                                   kb * kBlockK, b_row);
+                    } else if constexpr (kCluster == 2) {
+                        const uint32_t fb_leader = map_shared_rank(fb, leader);
                         tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
                         tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * kBlockK, b_row);
                     } else {
@@ -294,10 +319,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
+            GEMM_TR_SET(kTrEmptyWaitNs, empty_wait_ns);
+            (void)empty_wait_ns;
             // Every slot's last use must be released (the MMA's commit arrives
             // on this CTA's empty barriers) before the CTA may exit.
             for (int s = 0; s < kStages && ok; ++s) {
-                ok = wait_bounded<false>(empty_bar(stage), phase ^ 1u, abort_flag, p, 1, s);
+                ok = wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 1, s);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
         }
@@ -309,19 +336,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int i = 0;
+            uint64_t full_wait_ns = 0, acc_wait_ns = 0;   // trace builds only
             const int nwork = work_count(p.sched, pair_id);
             for (; i < nwork && ok; ++i) {
                 const Work w = work_item(p.sched, pair_id, i);
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
                 const uint64_t ta = GEMM_TR_NOW();
                 if (!wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i)) { ok = false; break; }
-                GEMM_TR_ADD(kTrAccEmptyWaitNs, GEMM_TR_NOW() - ta);
+                acc_wait_ns += GEMM_TR_NOW() - ta;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tf = GEMM_TR_NOW();
-                    if (!wait_bounded<false>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
-                    GEMM_TR_ADD(kTrFullWaitNs, GEMM_TR_NOW() - tf);
+                    if (!wait_bounded<(kCluster > 1)>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
+                    full_wait_ns += GEMM_TR_NOW() - tf;
                     if (i == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstFull);
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
@@ -332,16 +360,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
                         tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
                     }
-                    if constexpr (kPair == 2) tc_commit_pair(empty_bar(stage), 0x3);
+                    // release the slot in every CTA whose copies write into this pair's slot
+                    if constexpr (kCluster == 4) tc_commit_pair(empty_bar(stage), 0xF);
+                    else if constexpr (kCluster == 2) tc_commit_pair(empty_bar(stage), 0x3);
                     else tc_commit(empty_bar(stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), 0x3);
+                if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), (uint16_t)(0x3u << leader));
                 else tc_commit(accf_bar(b));
                 GEMM_TR_ITEM(kTrMmaEnd, i);
             }
             GEMM_TR(kTrWorkItems);
+            GEMM_TR_SET(kTrFullWaitNs, full_wait_ns);
+            GEMM_TR_SET(kTrAccEmptyWaitNs, acc_wait_ns);
+            (void)full_wait_ns;
+            (void)acc_wait_ns;
             // Both accumulators must be released by every epilogue warp of the
             // pair (the peer's arrive on this CTA's barriers) before exit.
             for (int j = 0; j < 2 && ok; ++j, ++i) {
@@ -398,7 +432,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tc_fence_after_sync();
             int mt, nt;
             tile_coords(p, w.tile, mt, nt);
-            const int row0 = mt * C::kTileM + (int)rank * kRowsPerCta + quad * 32;
+            const int row0 = mt * C::kTileM + (int)crank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
             if (w.ncontrib == 1) {
@@ -422,7 +456,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // and let the last contributor of the tile finish it.
                 const size_t part_stride = (size_t)kPartialFloats;
                 float4* mine = reinterpret_cast<float4*>(
-                    p.partials + ((size_t)(w.slot * kPair + (int)rank) * 4 + quad) * part_stride);
+                    p.partials + ((size_t)(w.slot * kCluster + (int)crank) * 4 + quad) * part_stride);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t v[32];
@@ -437,7 +471,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __threadfence();
                 __syncwarp();
                 if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrPartialDone, i);
-                int* counter = p.counters + (w.sk_index * 2 + (int)rank) * 4 + quad;
+                int* counter = p.counters + (w.sk_index * kCluster + (int)crank) * 4 + quad;
                 int prev = 0;
                 if (lane == 0) prev = atomicAdd(counter, 1);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
@@ -460,7 +494,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 } else {
                                     const float4* src = reinterpret_cast<const float4*>(
                                         p.partials +
-                                        ((size_t)(contributor_slot(p.sched, w.sk_index, k) * kPair + (int)rank) * 4 +
+                                        ((size_t)(contributor_slot(p.sched, w.sk_index, k) * kCluster + (int)crank) * 4 +
                                          quad) * part_stride);
 #pragma unroll
                                     for (int q = 0; q < 8; ++q) {
@@ -488,7 +522,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiEnd, i);
             if (lane == 0) {
-                if constexpr (kPair == 2) mbar_arrive_cluster(map_shared_rank(acce_bar(b), 0));
+                if constexpr (kPair == 2) mbar_arrive_cluster(map_shared_rank(acce_bar(b), leader));
                 else mbar_arrive_local(acce_bar(b));
             }
         }
@@ -509,7 +543,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         __syncthreads();
     }
-    if constexpr (kPair == 2) {
+    if constexpr (kCluster > 1) {
         cluster_arrive();
         cluster_wait();
     }

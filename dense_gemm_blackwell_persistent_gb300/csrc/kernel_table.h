@@ -1,6 +1,6 @@
 // kernel_table.h -- the instantiated variants of the persistent GEMM kernel.
 //
-// kernels_inst.cu is compiled once per (CTA pairing, output type); each
+// kernels_inst.cu is compiled once per (CTAs per unit, output type); each
 // object defines one lookup function over the tile widths.  The host side
 // (gemm_api.cu) picks a variant through gb300::kernel_info().
 #pragma once
@@ -20,25 +20,23 @@ struct KernelInfo {
 constexpr int kNumTileWidths = 5;
 constexpr int kTileWidths[kNumTileWidths] = {256, 224, 192, 160, 128};
 
-KernelInfo kernel_info_p1_o0(int bn);
-KernelInfo kernel_info_p1_o1(int bn);
-KernelInfo kernel_info_p1_o2(int bn);
-KernelInfo kernel_info_p2_o0(int bn);
-KernelInfo kernel_info_p2_o1(int bn);
-KernelInfo kernel_info_p2_o2(int bn);
+KernelInfo kernel_info_c1_o0(int bn);
+KernelInfo kernel_info_c1_o1(int bn);
+KernelInfo kernel_info_c1_o2(int bn);
+KernelInfo kernel_info_c2_o0(int bn);
+KernelInfo kernel_info_c2_o1(int bn);
+KernelInfo kernel_info_c2_o2(int bn);
+KernelInfo kernel_info_c4_o0(int bn);
+KernelInfo kernel_info_c4_o1(int bn);
+KernelInfo kernel_info_c4_o2(int bn);
 
-inline KernelInfo kernel_info(int pair, int bn, int out) {
-    if (pair == 1) {
-        switch (out) {
-            case 0: return kernel_info_p1_o0(bn);
-            case 1: return kernel_info_p1_o1(bn);
-            default: return kernel_info_p1_o2(bn);
-        }
-    }
-    switch (out) {
-        case 0: return kernel_info_p2_o0(bn);
-        case 1: return kernel_info_p2_o1(bn);
-        default: return kernel_info_p2_o2(bn);
+// cluster: CTAs per work unit (1, 2 or 4); out: 0 bf16, 1 f16, 2 fp32.
+inline KernelInfo kernel_info(int cluster, int bn, int out) {
+    switch (cluster) {
+        case 1: return out == 0 ? kernel_info_c1_o0(bn) : out == 1 ? kernel_info_c1_o1(bn) : kernel_info_c1_o2(bn);
+        case 2: return out == 0 ? kernel_info_c2_o0(bn) : out == 1 ? kernel_info_c2_o1(bn) : kernel_info_c2_o2(bn);
+        case 4: return out == 0 ? kernel_info_c4_o0(bn) : out == 1 ? kernel_info_c4_o1(bn) : kernel_info_c4_o2(bn);
+        default: return KernelInfo{nullptr, 0, 0};
     }
 }
 

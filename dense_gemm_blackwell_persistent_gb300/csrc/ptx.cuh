@@ -136,6 +136,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
+// Same as tma_load_2d_pair, and the box is also written to the same
+// shared-memory offset of every CTA in `cta_mask` (one L2 read, several
+// destinations).  Each destination's bytes complete on the barrier at
+// `bar`'s offset in the leader CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                           uint16_t cta_mask, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(cta_mask), "r"(c0), "r"(c1)
+        : "memory");
+}
 // 2-D tiled store shared -> global; elements outside the tensor are skipped.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1) {

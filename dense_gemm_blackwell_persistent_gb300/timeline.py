@@ -16,7 +16,8 @@ import json
 import numpy as np
 import torch
 
-from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_STREAM_K, GEMM_OPT_TILE_N, VARIANT,
+from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_MULTICAST, GEMM_OPT_STREAM_K, GEMM_OPT_TILE_N,
+               VARIANT,
                gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_run,
                gemm_plan_set_option, gemm_plan_trace)
 
@@ -64,7 +65,8 @@ def main():
     ap.add_argument("--out", type=int, default=0, help="0 bf16, 1 f16, 2 fp32")
     ap.add_argument("--pair", type=int, default=2)
     ap.add_argument("--tile-n", type=int, default=0)
-    ap.add_argument("--stream-k", type=int, default=1)
+    ap.add_argument("--stream-k", type=int, default=0)
+    ap.add_argument("--multicast", type=int, default=1)
     ap.add_argument("--max-ctas", type=int, default=0)
     ap.add_argument("--json", default="")
     a = ap.parse_args()
@@ -75,6 +77,7 @@ def main():
     gemm_plan_set_option(plan, GEMM_OPT_CTA_PAIR, a.pair)
     gemm_plan_set_option(plan, GEMM_OPT_TILE_N, a.tile_n)
     gemm_plan_set_option(plan, GEMM_OPT_STREAM_K, a.stream_k)
+    gemm_plan_set_option(plan, GEMM_OPT_MULTICAST, a.multicast)
     gemm_plan_set_option(plan, GEMM_OPT_MAX_CTAS, a.max_ctas)
     tin = torch.bfloat16 if a.dtype == 0 else torch.float16
     tout = {0: torch.bfloat16, 1: torch.float16, 2: torch.float32}[a.out]
@@ -90,7 +93,8 @@ def main():
     torch.cuda.synchronize()
     buf = gemm_plan_trace(plan)
     res = summarise(buf, gemm_plan_last_grid(plan))
-    print(f"{a.M}x{a.N}x{a.K} pair={a.pair} tile_n={a.tile_n or 256} stream_k={a.stream_k}: "
+    print(f"{a.M}x{a.N}x{a.K} pair={a.pair} multicast={a.multicast} tile_n={a.tile_n or 256} "
+          f"stream_k={a.stream_k}: "
           "[earliest, median, latest] µs over CTAs, count")
     for k, v in res.items():
         print(f"  {k:26s} {v}")

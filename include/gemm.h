@@ -72,9 +72,14 @@ typedef enum {
     GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
     GEMM_OPT_TILE_N = 4,         /* tile width: 256 (default, also 0), 224, 192, 160 or 128 */
-    GEMM_OPT_STREAM_K = 5        /* 1: spread the K work of a partial last wave over all
-                                    resident CTA pairs (stream-K tail, deterministic
+    GEMM_OPT_STREAM_K = 5,       /* 1: spread the K work of a partial last wave over all
+                                    resident units (stream-K tail, deterministic
                                     fixup); 0 (default): whole tiles only              */
+    GEMM_OPT_MULTICAST = 6       /* with CTA pairs: 1 = two pairs per 4-CTA cluster work
+                                    on vertically adjacent tiles and share their B tile
+                                    through TMA multicast (512×BN per cluster); 0 = one
+                                    pair per cluster; -1 (default) = multicast when the
+                                    rows of A and B are not a multiple of 128 bytes   */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan
@@ -118,6 +123,12 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
 
 /* Tile width BN the last run on this plan used (for reports). */
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);
+
+/* Launch configuration of the last run on this plan (for reports): CTAs
+ * launched, CTAs per work unit (1, 2 or 4), tile width, whole-tile waves and
+ * the number of tiles split along K by the stream-K tail. */
+int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* tile_n, int* dp_waves,
+                          int* sk_tiles);
 
 /* Timeline of the last runs, for builds compiled with GEMM_TRACE (other
  * builds return GEMM_ERR_UNSUPPORTED after filling *ctas and *slots).  Copies

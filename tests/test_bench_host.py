@@ -1,0 +1,71 @@
+"""bench.py host logic without a GPU: the multi-rank aggregation over a real
+two-rank gloo process group, and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r ran its 10 steps in (r + 1) * 100 ms; the job is timed by the slowest rank
+        value, ms_per_step = bench.aggregate(world, 1e12, 10, (rank + 1) * 100.0)
+        q.put((rank, bench.dist_info(), value, ms_per_step, bench.max_over_ranks(float(rank))))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, info, value, ms_per_step, mx in got:
+        assert info == (rank, rank, 2)
+        # 2 ranks × 10 steps × 1e12 FLOP over the slowest rank's 0.2 s
+        assert value == pytest.approx(2 * 10 * 1e12 / 0.2 / 1e12)
+        assert ms_per_step == pytest.approx(20.0)
+        assert mx == 1.0
+
+
+def test_aggregate_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    value, ms = bench.aggregate(1, 2e12, 4, 400.0)
+    assert value == pytest.approx(4 * 2e12 / 0.4 / 1e12) and ms == pytest.approx(100.0)
+
+
+def test_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "gemm_256_f32out", "--steps", "2", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "gemm_256_f32out"

@@ -45,6 +45,14 @@ def fresh_plan(g):
     g.gemm_plan_destroy(h)
 
 
+UNITS = [4, 2, 1]   # CTAs per work unit: multicast cluster of two pairs, one pair, one CTA
+
+
+def configure(g, plan, unit):
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 1 if unit == 1 else 2)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_MULTICAST, 1 if unit == 4 else 0)
+
+
 def run(g, plan, A, B, out_dtype, C=None):
     """C = A·Bᵀ through gemm_plan_run; C is poisoned with NaN first."""
     M, K = A.shape
@@ -72,12 +80,12 @@ def draw(M, N, K, dtype=wl.BF16, dist="normal", seed=0):
 
 # ------------------------------------------------------------------ bit-exact integer runs
 
-@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("unit", UNITS)
 @pytest.mark.parametrize("out", OUTS)
-@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 264), (384, 512, 1024)])
-def test_integer_inputs_bit_exact(g, plan, pair, out, shape):
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 264), (384, 512, 1024), (1100, 520, 136)])
+def test_integer_inputs_bit_exact(g, plan, unit, out, shape):
     M, N, K = shape
-    g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, pair)
+    configure(g, plan, unit)
     try:
         A, B = draw(M, N, K, dist="int", seed=0)
         C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), out))
@@ -88,7 +96,7 @@ def test_integer_inputs_bit_exact(g, plan, pair, out, shape):
             want = oracle.decode(oracle.encode(C_ref, out), out)
         assert np.array_equal(C, want), f"{int((C != want).sum())} mismatches"
     finally:
-        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 2)
+        configure(g, plan, 4)
 
 
 def test_integer_workload_256(g, plan):
@@ -115,51 +123,53 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("unit", UNITS)
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_shape_sweep(g, plan, pair, shape):
+def test_shape_sweep(g, plan, unit, shape):
     M, N, K = shape
-    g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, pair)
+    configure(g, plan, unit)
     try:
         for i, out in enumerate(OUTS):
             dtype = wl.BF16 if (i + M) % 2 == 0 else wl.F16
             A, B = draw(M, N, K, dtype=dtype, seed=M * 7 + N * 3 + K + i)
             C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), out))
             C_ref, S = oracle_full(A, B)
-            parity.assert_within(C, C_ref, S, out, f"{shape} pair={pair} out={out} in={dtype}")
+            parity.assert_within(C, C_ref, S, out, f"{shape} unit={unit} out={out} in={dtype}")
     finally:
-        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 2)
+        configure(g, plan, 4)
 
 
-@pytest.mark.parametrize("pair,ctas,group", [(2, 2, 8), (2, 6, 3), (1, 1, 8), (1, 5, 1), (2, 4, 1)])
-def test_persistent_loop_many_tiles(g, fresh_plan, pair, ctas, group):
+@pytest.mark.parametrize("unit,ctas,group", [(2, 2, 8), (2, 6, 3), (1, 1, 8), (1, 5, 1), (2, 4, 1),
+                                             (4, 4, 8), (4, 8, 1), (4, 12, 2)])
+def test_persistent_loop_many_tiles(g, fresh_plan, unit, ctas, group):
     """Few resident CTAs, many tiles each: wraps the shared-memory ring many
     times and alternates both TMEM accumulators across tiles."""
-    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+    configure(g, fresh_plan, unit)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, ctas)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_GROUP_M, group)
     M, N, K = 1100, 1288, 328
     for out in OUTS:
         A, B = draw(M, N, K, seed=ctas * 10 + group + out)
         C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
-        assert g.gemm_plan_last_grid(fresh_plan) == ctas // pair * pair
+        assert g.gemm_plan_last_grid(fresh_plan) == ctas // unit * unit
         C_ref, S = oracle_full(A, B)
-        parity.assert_within(C, C_ref, S, out, f"pair={pair} ctas={ctas} group={group} out={out}")
+        parity.assert_within(C, C_ref, S, out, f"unit={unit} ctas={ctas} group={group} out={out}")
 
 
 TILE_NS = [256, 224, 192, 160, 128]
 
 
 
-@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("unit", UNITS)
 @pytest.mark.parametrize("tile_n", TILE_NS)
-def test_every_tile_width(g, fresh_plan, pair, tile_n):
-    """Each instantiated tile width, both pairings, all output types: ragged in
-    M, N and K, several tiles in each direction, few CTAs so each walks many
-    tiles; integer inputs bit-exact, random inputs within tolerance."""
-    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+def test_every_tile_width(g, fresh_plan, unit, tile_n):
+    """Each instantiated tile width, every unit size, all output types: ragged
+    in M, N and K, several tiles in each direction, few CTAs so each walks
+    many tiles; integer inputs bit-exact, random inputs within tolerance."""
+    configure(g, fresh_plan, unit)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, tile_n)
-    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, 4)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, 8)
+    pair = unit
     M, N, K = 600, 1000, 392
     for out in OUTS:
         A, B = draw(M, N, K, dist="int", seed=tile_n + out)
@@ -188,17 +198,18 @@ def test_default_tile_width_is_full(g, plan):
 
 # (M, N, K, max CTAs): shapes whose last wave is split along K over all units
 STREAM_K_CASES = [
-    (1024, 1280, 1024, 0),   # 20 tiles over every resident pair: ~4 contributors per tile
-    (700, 1000, 1000, 10),   # 12 tiles on 5 pairs: 2 full waves + 2 split tiles
-    (520, 776, 2056, 6),     # 3 pairs, ragged M/N/K
+    (1024, 1280, 1024, 0),   # fewer tiles than units: every tile split over ~4 units
+    (1300, 1000, 1000, 12),  # few units: full waves + split tiles
+    (520, 776, 2056, 8),     # ragged M/N/K
 ]
 
 
-@pytest.mark.parametrize("pair", [2, 1])
+@pytest.mark.parametrize("unit", UNITS)
 @pytest.mark.parametrize("case", STREAM_K_CASES, ids=lambda c: "x".join(map(str, c)))
-def test_stream_k_tail(g, fresh_plan, pair, case):
+def test_stream_k_tail(g, fresh_plan, unit, case):
     M, N, K, ctas = case
-    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, pair)
+    configure(g, fresh_plan, unit)
+    pair = unit
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, ctas)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STREAM_K, 1)
     for out in OUTS:
