@@ -158,10 +158,28 @@ int resident_units(const gemm_plan* plan, int cluster) {
     return std::max(1, units);
 }
 
-// Tile width.  One tcgen05.mma occupies the tensor pipe for about the same
-// time for every N from 128 to 256 (measured on GB300), so the full width of
-// 256 is the fast choice; narrower widths stay available as an option.
-int choose_tile_n(const gemm_plan* plan) { return plan->tile_n > 0 ? plan->tile_n : kTileWidths[0]; }
+// Tile width: the candidate that minimises (waves of resident units) ×
+// (BN + 48).  The per-K-block time of the kernel measured on GB300 grows as
+// BN + 48 (316 / 242 / 183 ns for BN = 256 / 192 / 128 with CTA pairs at
+// 8192³), so a narrower tile pays off when it fills the last wave: 224 at
+// 4096³ (4 full waves instead of 3.4) and at 1024×4096×4096.
+int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster) {
+    if (plan->tile_n > 0) return plan->tile_n;
+    const int64_t units = resident_units(plan, cluster);
+    const int64_t tiles_m = (M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster);
+    int best = kTileWidths[0];
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < kNumTileWidths; ++i) {
+        const int bn = kTileWidths[i];
+        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + units - 1) / units) * (bn + 48);
+        if (cost < best_cost) {   // ties keep the wider tile
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
            int out_dtype, cudaStream_t stream) {
@@ -173,7 +191,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     }
     const int pair = plan->pair;
     const int cluster = unit_ctas(plan, K);
-    const int bn = choose_tile_n(plan);
+    const int bn = choose_tile_n(plan, M, N, cluster);
     const KernelInfo ki = kernel_info(cluster, bn, out_dtype);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * cluster;

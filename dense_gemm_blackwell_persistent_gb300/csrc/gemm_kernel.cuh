@@ -275,9 +275,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
     if (threadIdx.x == 0) GEMM_TR(kTrSetup);
 
+    // The producer and MMA loops run on the whole warp, so that stage, phase
+    // and the descriptors stay warp-uniform (the TMA and tcgen05.mma operands
+    // live in uniform registers); one elected lane issues the instructions.
+    // A single-lane loop in a divergent branch measured ~25% slower per K
+    // block on GB300.
     if (warp == 0) {
         // ================= TMA producer
-        if (lane == 0) {
+        {
+            const bool issuer = elect_one_sync();
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             uint64_t empty_wait_ns = 0;   // trace builds only
@@ -290,32 +296,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tw = GEMM_TR_NOW();
-                    if (!wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb)) {
+                    if (!__all_sync(0xffffffffu,
+                                    wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb))) {
                         ok = false;
                         break;
                     }
                     empty_wait_ns += GEMM_TR_NOW() - tw;
                     if (j == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstLoad);
                     const uint32_t fb = full_bar(stage);
-                    if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
                     const uint32_t a_dst = base + stage * kStageBytesA;
                     const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
-                    if constexpr (kCluster == 4) {
-                        // own A rows; a quarter of the pair-tile's B rows, written to
-                        // this CTA and to the same-rank CTA of the other pair
-                        const uint32_t fb_leader = map_shared_rank(fb, leader);
-                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-                        tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
-                        tma_load_2d_pair_multicast(b_dst + pidx * C::kLoadBytesB, &tmB, fb_leader, mask,
-                                                   kb * kBlockK, b_row);
-                    } else if constexpr (kCluster == 2) {
-                        const uint32_t fb_leader = map_shared_rank(fb, leader);
-                        tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
-                        tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * kBlockK, b_row);
-                    } else {
-                        tma_load_2d(a_dst, &tmA, fb, kb * kBlockK, a_row);
-                        tma_load_2d(b_dst, &tmB, fb, kb * kBlockK, b_row);
+                    if (issuer) {
+                        if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
+                        if constexpr (kCluster == 4) {
+                            // own A rows; a quarter of the pair-tile's B rows, written to
+                            // this CTA and to the same-rank CTA of the other pair
+                            const uint32_t fb_leader = map_shared_rank(fb, leader);
+                            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
+                            tma_load_2d_pair_multicast(b_dst + pidx * C::kLoadBytesB, &tmB, fb_leader, mask,
+                                                       kb * kBlockK, b_row);
+                        } else if constexpr (kCluster == 2) {
+                            const uint32_t fb_leader = map_shared_rank(fb, leader);
+                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
+                            tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * kBlockK, b_row);
+                        } else {
+                            tma_load_2d(a_dst, &tmA, fb, kb * kBlockK, a_row);
+                            tma_load_2d(b_dst, &tmB, fb, kb * kBlockK, b_row);
+                        }
                     }
+                    __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -324,14 +334,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // Every slot's last use must be released (the MMA's commit arrives
             // on this CTA's empty barriers) before the CTA may exit.
             for (int s = 0; s < kStages && ok; ++s) {
-                ok = wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 1, s);
+                ok = __all_sync(0xffffffffu, wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 1, s));
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================= MMA issuer (leader CTA only)
-        if (rank == 0 && lane == 0) {
+        if (rank == 0) {
+            const bool issuer = elect_one_sync();
             const uint32_t a_base = base, b_base = base + C::kOffB;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
@@ -342,33 +353,45 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const Work w = work_item(p.sched, pair_id, i);
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
                 const uint64_t ta = GEMM_TR_NOW();
-                if (!wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i))) {
+                    ok = false;
+                    break;
+                }
                 acc_wait_ns += GEMM_TR_NOW() - ta;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tf = GEMM_TR_NOW();
-                    if (!wait_bounded<(kCluster > 1)>(full_bar(stage), phase, abort_flag, p, 3, kb)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, wait_bounded<(kCluster > 1)>(full_bar(stage), phase, abort_flag, p, 3, kb))) {
+                        ok = false;
+                        break;
+                    }
                     full_wait_ns += GEMM_TR_NOW() - tf;
                     if (i == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstFull);
-                    tc_fence_after_sync();
                     const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
                     const uint64_t bd = smem_desc_sw128(b_base + stage * C::kStageBytesB);
                     const uint32_t first = kb == w.kb_begin;
+                    if (issuer) {
+                        tc_fence_after_sync();
 #pragma unroll
-                    for (int j = 0; j < kBlockK / kMmaK; ++j) {
-                        // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
-                        tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
+                        for (int j = 0; j < kBlockK / kMmaK; ++j) {
+                            // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
+                            tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
+                        }
+                        // release the slot in every CTA whose copies write into this pair's slot
+                        if constexpr (kCluster == 4) tc_commit_pair(empty_bar(stage), 0xF);
+                        else if constexpr (kCluster == 2) tc_commit_pair(empty_bar(stage), 0x3);
+                        else tc_commit(empty_bar(stage));
                     }
-                    // release the slot in every CTA whose copies write into this pair's slot
-                    if constexpr (kCluster == 4) tc_commit_pair(empty_bar(stage), 0xF);
-                    else if constexpr (kCluster == 2) tc_commit_pair(empty_bar(stage), 0x3);
-                    else tc_commit(empty_bar(stage));
+                    __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), (uint16_t)(0x3u << leader));
-                else tc_commit(accf_bar(b));
+                if (issuer) {
+                    if constexpr (kPair == 2) tc_commit_pair(accf_bar(b), (uint16_t)(0x3u << leader));
+                    else tc_commit(accf_bar(b));
+                }
+                __syncwarp();
                 GEMM_TR_ITEM(kTrMmaEnd, i);
             }
             GEMM_TR(kTrWorkItems);
@@ -379,7 +402,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             // Both accumulators must be released by every epilogue warp of the
             // pair (the peer's arrive on this CTA's barriers) before exit.
             for (int j = 0; j < 2 && ok; ++j, ++i) {
-                ok = wait_bounded<true>(acce_bar(i & 1), ((i >> 1) & 1) ^ 1u, abort_flag, p, 4, j);
+                ok = __all_sync(0xffffffffu, wait_bounded<true>(acce_bar(i & 1), ((i >> 1) & 1) ^ 1u, abort_flag, p, 4, j));
             }
         }
         __syncwarp();

@@ -71,7 +71,8 @@ typedef enum {
                                     1: one CTA per 128×BN tile                          */
     GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
-    GEMM_OPT_TILE_N = 4,         /* tile width: 256 (default, also 0), 224, 192, 160 or 128 */
+    GEMM_OPT_TILE_N = 4,         /* tile width: 256, 224, 192, 160 or 128 (0 = default:
+                                    chosen per problem to fill whole waves)             */
     GEMM_OPT_STREAM_K = 5,       /* 1: spread the K work of a partial last wave over all
                                     resident units (stream-K tail, deterministic
                                     fixup); 0 (default): whole tiles only              */

@@ -185,15 +185,19 @@ def test_every_tile_width(g, fresh_plan, unit, tile_n):
         parity.assert_within(C, C_ref, S, out, f"tile_n={tile_n} pair={pair} out={out}")
 
 
-def test_default_tile_width_is_full(g, plan):
-    """Every tcgen05.mma occupies the tensor pipe about equally long for N in
-    128..256, so the default tile is the full 256 columns."""
-    w = wl.WORKLOADS["gemm_4096_bf16"]
+@pytest.mark.parametrize("name,expect", [("gemm_4096_bf16", 224), ("gemm_1024x4096x4096_f16", 224),
+                                         ("gemm_8192_bf16", 256)])
+def test_tile_width_choice_fills_waves(g, plan, name, expect):
+    """The host picks the width that minimises waves × (width + 48): a
+    narrower tile when it turns a partial last wave into whole waves."""
+    w = wl.WORKLOADS[name]
     A = torch.zeros((w.M, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
     B = torch.zeros((w.N, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
     C = run(g, plan, A, B, w.out_dtype)
     assert bool((C == 0).all())
-    assert g.gemm_plan_last_tile_n(plan) == 256
+    launch = g.gemm_plan_last_launch(plan)
+    if launch["ctas"] == 152 and launch["ctas_per_unit"] == 2:
+        assert launch["tile_n"] == expect, launch
 
 
 # (M, N, K, max CTAs): shapes whose last wave is split along K over all units
