@@ -66,11 +66,16 @@ constexpr int kTraceSlots = 64;
 enum TraceSlot {
     kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrFirstFull = 3, kTrTeardown = 4, kTrExit = 5,
     kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8, kTrWorkItems = 9,
+    kTrFirstItem = 10,    // producer: first work item decoded
+    kTrEpiDone = 11,      // epilogue warp 2: all stores of the CTA complete
+    kTrClusterArrived = 12, kTrClusterDone = 13, kTrDealloc = 14,
     kTrMmaEnd = 16,       // + item (8 items)
     kTrEpiStart = 24,     // + item
     kTrEpiEnd = 32,       // + item
     kTrPartialDone = 40,  // + item: stream-K partial published
     kTrReduceDone = 48,   // + item: stream-K reduction finished (last contributor)
+    kTrClkFirstFull = 15, // SM clock cycles (clock64) at first_full ...
+    kTrClkMmaEnd = 56,    // ... and at mma_end + item: cycles per k-block
 };
 #ifdef GEMM_TRACE
 #define GEMM_TR(slot) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
@@ -96,7 +101,9 @@ constexpr int kChunkCols = 32;           // accumulator columns per epilogue sto
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any single wait
 
 constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2;
+constexpr int kErrCuda = -4;      // device side: the launch's shared memory is not 1 KB aligned
 constexpr int kErrTimeout = -7;
+constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the base address
 
 struct Params {
     int M, N, K;
@@ -136,7 +143,7 @@ struct Cfg {
     static constexpr int kSlotBytes = 32 * kRowBytes;           // one 32-row store box
     static constexpr int kStagingBytes = kEpiWarps * 2 * kSlotBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kFixed = kStagingBytes + kBarBytes + 16 + 1024;  // + slack to align the base
+    static constexpr int kFixed = kStagingBytes + kBarBytes + 16;
     static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static_assert(kStages >= 3, "ring too shallow");
@@ -144,7 +151,7 @@ struct Cfg {
     static constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
     static constexpr int kOffBars = kOffStaging + kStagingBytes;
     static constexpr int kOffMisc = kOffBars + kBarBytes;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr int kSmemBytes = kOffMisc + 16;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert((2 * kStages + 4) * 8 <= kBarBytes, "barrier area");
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
@@ -176,8 +183,8 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mt, int
     nt = r / gsize;
 }
 
-__device__ __forceinline__ void record_error(const Params& p, int role, int detail) {
-    if (atomicCAS(p.status, 0, kErrTimeout) == 0) {
+__device__ __forceinline__ void record_error(const Params& p, int role, int detail, int code = kErrTimeout) {
+    if (atomicCAS(p.status, 0, code) == 0) {
         p.status[1] = role;
         p.status[2] = (int)blockIdx.x;
         p.status[3] = detail;
@@ -222,11 +229,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     constexpr int kStages = C::kStages;
     constexpr int kChunks = kBN / kChunkCols;
 
-    extern __shared__ uint8_t smem_raw[];
+    // The 128-byte-swizzled operand tiles need 1 KB alignment.  The dynamic
+    // shared window is declared 1 KB aligned rather than padded by 1 KB:
+    // that padding is what a 7th ring slot of a 256x224 tile needs.  Every
+    // CTA of the launch has the same layout, so if the window were ever
+    // misaligned all of them would record the error and return here,
+    // before touching any barrier, TMEM or cluster peer.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (threadIdx.x == 0) GEMM_TR(kTrEntry);
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    uint8_t* smem = smem_raw + (base - raw_addr);
+    const uint32_t base = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw;
+    if (base & 1023u) {
+        if (threadIdx.x == 0) record_error(p, kRoleSmemBase, (int)base, kErrCuda);
+        return;
+    }
 
     const uint32_t bars = base + C::kOffBars;
     auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -242,6 +258,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t pidx = crank / kPair;                             // which pair of the unit
     const uint32_t leader = crank & ~(uint32_t)(kPair - 1);          // cluster rank of this pair's leader
     const int pair_id = kCluster > 1 ? (int)cluster_id_x() : (int)blockIdx.x;   // work unit
+
+    // Operand rows of this CTA for output tile `tile` (A: its 128 rows; B: the
+    // rows of the pair's B tile that this CTA loads).
+    auto operand_rows = [&](int tile, int& a_row, int& b_row) {
+        int mt, nt;
+        tile_coords(p, tile, mt, nt);
+        a_row = mt * C::kTileM + (int)crank * kRowsPerCta;
+        b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
+    };
 
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
@@ -261,18 +286,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmC);
     }
+    // The barrier inits are published CTA-wide and to the peer CTAs by the
+    // cluster barrier (a CTA barrier without a cluster).  The MMA warp
+    // arrives on it before allocating TMEM and waits after, so the producer's
+    // first loads do not wait for the allocation; the TMEM address reaches
+    // the epilogue warps through a named barrier of warps 1-5.
+    if constexpr (kCluster > 1) cluster_arrive();
+    else __syncthreads();
     if (warp == 1) {
         tmem_alloc<kPair>(smem_addr(tmem_holder), kTmemCols);
         tmem_relinquish<kPair>();
     }
-    tc_fence_before_sync();
-    __syncthreads();
-    if constexpr (kCluster > 1) {
-        cluster_arrive();
-        cluster_wait();
+    if constexpr (kCluster > 1) cluster_wait();
+    uint32_t tmem_base = 0;
+    if (warp >= 1) {
+        tc_fence_before_sync();
+        named_bar_sync(1, kNumThreads - 32);
+        tc_fence_after_sync();
+        tmem_base = *tmem_holder;
     }
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_holder;
     if (threadIdx.x == 0) GEMM_TR(kTrSetup);
 
     // The producer and MMA loops run on the whole warp, so that stage, phase
@@ -290,10 +322,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int nwork = work_count(p.sched, pair_id);
             for (int j = 0; j < nwork && ok; ++j) {
                 const Work w = work_item(p.sched, pair_id, j);
-                int mt, nt;
-                tile_coords(p, w.tile, mt, nt);
-                const int a_row = mt * C::kTileM + (int)crank * kRowsPerCta;
-                const int b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
+                int a_row, b_row;
+                operand_rows(w.tile, a_row, b_row);
+                if (j == 0 && lane == 0) GEMM_TR(kTrFirstItem);
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tw = GEMM_TR_NOW();
                     if (!__all_sync(0xffffffffu,
@@ -367,7 +398,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     full_wait_ns += GEMM_TR_NOW() - tf;
-                    if (i == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstFull);
+                    if (i == 0 && kb == w.kb_begin) {
+                        GEMM_TR(kTrFirstFull);
+                        GEMM_TR_SET(kTrClkFirstFull, (unsigned long long)clock64());
+                    }
                     const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
                     const uint64_t bd = smem_desc_sw128(b_base + stage * C::kStageBytesB);
                     const uint32_t first = kb == w.kb_begin;
@@ -393,6 +427,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 __syncwarp();
                 GEMM_TR_ITEM(kTrMmaEnd, i);
+                if (i < 8) GEMM_TR_SET(kTrClkMmaEnd + i, (unsigned long long)clock64());
             }
             GEMM_TR(kTrWorkItems);
             GEMM_TR_SET(kTrFullWaitNs, full_wait_ns);
@@ -464,6 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // while chunk c is converted, staged and stored.
                     uint32_t ra[32], rb[32];
                     tmem_ld_32x32b_x32(t_row, ra);
+                    tmem_ld_wait(ra);
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c) {
                         uint32_t(&cur)[32] = (c & 1) ? rb : ra;
@@ -471,8 +507,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
                         const int ccol = col0 + c * kChunkCols;
                         if (ccol < p.N) store_chunk(cur, ccol, row0);
+                        if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
-                    tmem_ld_wait();
                 }
             } else {
                 // Stream-K segment: publish this partial, count the arrival,
@@ -484,13 +520,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c * kChunkCols, v);
+                    tmem_ld_wait(v);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         __stcg(&mine[(c * 8 + q) * 32 + lane],
                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                 }
-                tmem_ld_wait();
                 __threadfence();
                 __syncwarp();
                 if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrPartialDone, i);
@@ -507,7 +543,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             if (ccol >= p.N) break;
                             uint32_t own[32];
                             tmem_ld_32x32b_x32(t_row + c * kChunkCols, own);
-                            tmem_ld_wait();
+                            tmem_ld_wait(own);
                             float acc[32];
                             for (int k = 0; k < w.ncontrib; ++k) {   // contributor order: fixed sum order
                                 float part[32];
@@ -551,6 +587,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
+        if (warp == 2 && lane == 0) GEMM_TR(kTrEpiDone);
     }
 
     // ---- teardown
@@ -568,11 +605,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     if constexpr (kCluster > 1) {
         cluster_arrive();
+        if (threadIdx.x == 0) GEMM_TR(kTrClusterArrived);
         cluster_wait();
+        if (threadIdx.x == 0) GEMM_TR(kTrClusterDone);
     }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<kPair>(tmem_base, kTmemCols);
+        if (lane == 0) GEMM_TR(kTrDealloc);
     }
     if (threadIdx.x == 0) GEMM_TR(kTrExit);
 }

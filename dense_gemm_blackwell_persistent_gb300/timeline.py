@@ -7,6 +7,11 @@ Runs a few warm-up launches, clears the trace, runs one launch and prints,
 for every trace point, the earliest / median / latest time over the CTAs
 (µs from the first CTA's entry) and the per-CTA wait totals.  --json writes
 the same summary to a file.
+
+Timer reads are not ordered against barriers by the compiler: a point taken
+right after a __syncthreads (teardown) can carry the time at which the
+recording thread reached the barrier, not when it left it.  The epilogue's
+own points (epi_end, epilogue_stores_done) bound the end of the work.
 """
 from __future__ import annotations
 
@@ -18,10 +23,12 @@ import torch
 
 from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_MULTICAST, GEMM_OPT_STREAM_K, GEMM_OPT_TILE_N,
                VARIANT,
-               gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_run,
+               gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_last_launch, gemm_plan_run,
                gemm_plan_set_option, gemm_plan_trace)
 
-POINTS = {0: "entry", 1: "setup_done", 2: "first_load_issued", 3: "first_full", 4: "teardown", 5: "exit"}
+POINTS = {0: "entry", 1: "setup_done", 10: "first_item_decoded", 2: "first_load_issued", 3: "first_full",
+          11: "epilogue_stores_done", 4: "teardown", 12: "cluster_arrived", 13: "cluster_done", 14: "tmem_dealloc",
+          5: "exit"}
 ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published", 48: "reduce_done"}
 TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us"}
 
@@ -48,6 +55,19 @@ def summarise(buf: np.ndarray, ctas: int) -> dict:
             s = stats(base + j)
             if s:
                 out[f"{name}[{j}]"] = s
+    # SM clock: cycles and ns between first_full and each mma_end of the
+    # pair leaders give the clock and the cycles per k-block of each item.
+    lead = t[:, 15] > 0
+    if lead.any():
+        c0, n0 = t[lead, 15], t[lead, 3]
+        for j in range(8):
+            cj, nj = t[lead, 56 + j], t[lead, 16 + j]
+            ok = (cj > 0) & (nj > 0)
+            if not ok.any():
+                break
+            mhz = (cj[ok] - c0[ok]) / np.maximum(nj[ok] - n0[ok], 1) * 1e3
+            out[f"sm_mhz_to_mma_end[{j}]"] = round(float(np.median(mhz)), 1)
+            out[f"cycles_first_full_to_mma_end[{j}]"] = int(np.median(cj[ok] - c0[ok]))
     for col, name in TOTALS.items():
         v = t[:, col][t[:, col] > 0] / 1e3
         if v.size:
@@ -66,8 +86,9 @@ def main():
     ap.add_argument("--pair", type=int, default=2)
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stream-k", type=int, default=0)
-    ap.add_argument("--multicast", type=int, default=1)
+    ap.add_argument("--multicast", type=int, default=-1, help="-1 auto, 0 off, 1 on")
     ap.add_argument("--max-ctas", type=int, default=0)
+    ap.add_argument("--no-flush", action="store_true", help="keep the operands in L2 before the traced launch")
     ap.add_argument("--json", default="")
     a = ap.parse_args()
     if VARIANT != "trace":
@@ -89,12 +110,15 @@ def main():
         gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), a.M, a.N, a.K, a.dtype, a.out, s)
     torch.cuda.synchronize()
     gemm_plan_trace(plan)
+    if not a.no_flush:
+        torch.empty(512 << 20, dtype=torch.uint8, device="cuda").zero_()   # evict A, B, C from L2
     gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), a.M, a.N, a.K, a.dtype, a.out, s)
     torch.cuda.synchronize()
     buf = gemm_plan_trace(plan)
     res = summarise(buf, gemm_plan_last_grid(plan))
-    print(f"{a.M}x{a.N}x{a.K} pair={a.pair} multicast={a.multicast} tile_n={a.tile_n or 256} "
-          f"stream_k={a.stream_k}: "
+    launch = gemm_plan_last_launch(plan)
+    print(f"{a.M}x{a.N}x{a.K} unit={launch['ctas_per_unit']} tile_n={launch['tile_n']} ctas={launch['ctas']} "
+          f"stream_k={a.stream_k} l2={'warm' if a.no_flush else 'flushed'}: "
           "[earliest, median, latest] µs over CTAs, count")
     for k, v in res.items():
         print(f"  {k:26s} {v}")

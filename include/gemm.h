@@ -55,7 +55,9 @@ typedef enum {
     GEMM_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad dtype pair, bad option */
     GEMM_ERR_UNSUPPORTED = -2,   /* shape/pitch TMA cannot address (see layout rules)       */
     GEMM_ERR_MISALIGNED = -3,    /* a pointer not 16-byte aligned                            */
-    GEMM_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute, copy)     */
+    GEMM_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute, copy);
+                                    device side: the launch's shared memory was not 1 KB
+                                    aligned (see gemm_plan_status)                        */
     GEMM_ERR_DRIVER = -5,        /* the driver's tensor-map encoder failed or is missing     */
     GEMM_ERR_NO_PLAN = -6,       /* gemm_run with no plan created for the current device     */
     GEMM_ERR_TIMEOUT = -7,       /* device side: a bounded wait expired (see gemm_plan_status) */
