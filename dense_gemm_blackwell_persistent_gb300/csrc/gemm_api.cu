@@ -106,8 +106,8 @@ struct gemm_plan {
     int cap_ctas = 0;
     int tile_n = 0;               // 0 = 256
     int stream_k = 0;             // split the K work of a partial last wave (option)
-    float* d_partials = nullptr;  // stream-K workspace: 2 slots per unit
-    int* d_counters = nullptr;    // stream-K arrival counters
+    float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
+    int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
     int* d_status = nullptr;      // 4 ints, see Params::status
     int last_grid = 0;
@@ -210,11 +210,10 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     // Stream-K spreads a partial last wave over every resident unit; with
     // whole tiles only, never launch more units than tiles.
     const int resident = resident_units(plan, cluster);
-    const bool sk = plan->stream_k && plan->d_partials != nullptr && plan->d_counters != nullptr;
+    const bool sk = plan->stream_k && plan->d_partials != nullptr && plan->d_flags != nullptr;
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
-    if (p.sched.sk_tiles == 0) p.sched = make_schedule(p.num_tiles, std::min(resident, p.num_tiles), p.k_blocks, false);
     p.partials = plan->d_partials;
-    p.counters = plan->d_counters;
+    p.flags = plan->d_flags;
     p.trace = plan->d_trace;
 
     CUtensorMap tmA, tmB, tmC;
@@ -264,13 +263,14 @@ int max_resident_ctas(const gemm_plan* plan) {
     return std::max(plan->max_ctas[1], std::max(plan->max_ctas[2], plan->max_ctas[4]));
 }
 
+// One partial slot per unit: 4 epilogue warps × 32 rows × 256 fp32 per CTA.
 size_t partials_bytes(const gemm_plan* plan) {
     const int ctas = max_resident_ctas(plan);
-    return (size_t)2 * ctas * 4 * kPartialFloats * sizeof(float);
+    return (size_t)ctas * 4 * kPartialFloats * sizeof(float);
 }
-// One counter per (tail tile, CTA of the pair, epilogue warp); a tail has
-// fewer tiles than units.
-size_t counters_bytes(const gemm_plan* plan) {
+// One flag per (split tile, CTA of the unit, epilogue warp); the stream-K
+// part has fewer than twice as many tiles as units.
+size_t flags_bytes(const gemm_plan* plan) {
     const int ctas = max_resident_ctas(plan);
     return (size_t)ctas * 2 * 4 * sizeof(int);
 }
@@ -348,8 +348,8 @@ int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
     if (rc == GEMM_OK && cudaMalloc(&plan->d_status, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMemset(plan->d_status, 0, 4 * sizeof(int)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMalloc(&plan->d_partials, partials_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
-    if (rc == GEMM_OK && cudaMalloc(&plan->d_counters, counters_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
-    if (rc == GEMM_OK && cudaMemset(plan->d_counters, 0, counters_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMalloc(&plan->d_flags, flags_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
+    if (rc == GEMM_OK && cudaMemset(plan->d_flags, 0, flags_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
 #ifdef GEMM_TRACE
     if (rc == GEMM_OK && cudaMalloc(&plan->d_trace, trace_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
     if (rc == GEMM_OK && cudaMemset(plan->d_trace, 0, trace_bytes(plan)) != cudaSuccess) rc = GEMM_ERR_CUDA;
@@ -358,7 +358,7 @@ int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
         cudaGetLastError();
         if (plan->d_status) cudaFree(plan->d_status);
         if (plan->d_partials) cudaFree(plan->d_partials);
-        if (plan->d_counters) cudaFree(plan->d_counters);
+        if (plan->d_flags) cudaFree(plan->d_flags);
         delete plan;
         cudaSetDevice(prev);
         return rc;
@@ -487,9 +487,9 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status) {
         return GEMM_ERR_CUDA;
     }
     *device_status = h[0];
-    // A run that gave up part-way may leave stream-K counters non-zero.
-    if (h[0] != 0 && plan->d_counters != nullptr &&
-        cudaMemset(plan->d_counters, 0, counters_bytes(plan)) != cudaSuccess) {
+    // A run that gave up part-way may leave stream-K flags raised.
+    if (h[0] != 0 && plan->d_flags != nullptr &&
+        cudaMemset(plan->d_flags, 0, flags_bytes(plan)) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -549,7 +549,7 @@ int gemm_plan_destroy(gemm_plan_t plan) {
     cudaSetDevice(plan->device);
     if (plan->d_status) cudaFree(plan->d_status);
     if (plan->d_partials) cudaFree(plan->d_partials);
-    if (plan->d_counters) cudaFree(plan->d_counters);
+    if (plan->d_flags) cudaFree(plan->d_flags);
     if (plan->d_trace) cudaFree(plan->d_trace);
     for (int i = 0; i < 3; ++i)
         if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);

@@ -110,15 +110,16 @@ struct Params {
     int tiles_m, tiles_n, k_blocks, num_tiles, group_m;
     uint32_t idesc;
     int* status;       // [0] first error code, [1] role, [2] block, [3] detail
-    Schedule sched;    // data-parallel waves + stream-K tail
-    float* partials;   // stream-K partial tiles (2 slots per unit), or null
-    int* counters;     // stream-K arrival counters per (tail tile, CTA, quadrant)
+    Schedule sched;    // whole-tile waves + stream-K part
+    float* partials;   // stream-K: one partial-tile slot per unit, or null
+    int* flags;        // stream-K: "partial published" per (split tile, CTA, epilogue warp)
     unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
 };
 
 // fp32 partial of one epilogue warp: 32 rows × 256 columns, stored as
 // float4 groups [column/4][row] so that a warp's accesses are contiguous.
 constexpr int kPartialFloats = 32 * 256;
+constexpr int kFixupBytes = kPartialFloats * 4;   // shared memory per epilogue warp for a fix-up
 
 // kCluster: CTAs per work unit -- 1 (one CTA, tcgen05 cta_group::1), 2 (a
 // CTA pair issuing cta_group::2 MMAs) or 4 (two pairs stacked along M that
@@ -153,7 +154,9 @@ struct Cfg {
     static constexpr int kOffMisc = kOffBars + kBarBytes;
     static constexpr int kSmemBytes = kOffMisc + 16;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert((2 * kStages + 4) * 8 <= kBarBytes, "barrier area");
+    static_assert((2 * kStages + 4 + kEpiWarps) * 8 <= kBarBytes, "barrier area");
+    static constexpr uint32_t kPartialBytes = kBN * 32 * 4;   // one epilogue warp's fp32 partial
+    static_assert(kEpiWarps * kFixupBytes <= kOffStaging, "fix-up buffers must fit in the operand ring");
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
     static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // bytes landing in a pair, tracked by its leader
 };
@@ -210,6 +213,32 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Wait until *flag == 1 (another CTA's release), for at most kWaitLimitNs:
+// lane 0 polls, the warp gets the outcome.  On expiry records a timeout and
+// raises the CTA's abort flag; gives up early if another role aborted.
+__device__ __forceinline__ bool wait_flag_bounded(const int* flag, volatile uint32_t* abort_flag, const Params& p,
+                                                  int role, int detail) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_gpu(flag) != 1) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            __nanosleep(100);
+            if (ld_acquire_gpu(flag) == 1) break;
+            if (*abort_flag) {
+                ok = 0;
+                break;
+            }
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                record_error(p, role, detail);
+                *abort_flag = 1;
+                ok = 0;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
     if (out == kOutBF16) {
         __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -249,6 +278,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
     auto accf_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };
+    auto fix_bar = [&](int e) { return bars + 8u * (2 * kStages + 4 + e); };   // per epilogue warp
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
 
@@ -278,6 +308,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), kEpiWarps * kPair);
         }
+        for (int e = 0; e < kEpiWarps; ++e) mbar_init(fix_bar(e), 1);
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -510,12 +541,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
                 }
-            } else {
-                // Stream-K segment: publish this partial, count the arrival,
-                // and let the last contributor of the tile finish it.
-                const size_t part_stride = (size_t)kPartialFloats;
+            } else if (w.contrib == 1) {
+                // Second piece of a split tile: publish the fp32 partial in
+                // this unit's workspace slot, then raise this warp's flag.
                 float4* mine = reinterpret_cast<float4*>(
-                    p.partials + ((size_t)(w.slot * kCluster + (int)crank) * 4 + quad) * part_stride);
+                    p.partials + ((size_t)(w.slot * kCluster + (int)crank) * 4 + quad) * kPartialFloats);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t v[32];
@@ -527,55 +557,58 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                 }
+                fence_proxy_async_global();   // the finisher reads the partial with a bulk copy
                 __threadfence();
                 __syncwarp();
+                if (lane == 0) st_release_gpu(p.flags + (w.sk_index * kCluster + (int)crank) * 4 + quad, 1);
                 if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrPartialDone, i);
-                int* counter = p.counters + (w.sk_index * kCluster + (int)crank) * 4 + quad;
-                int prev = 0;
-                if (lane == 0) prev = atomicAdd(counter, 1);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == w.ncontrib - 1) {
-                    __threadfence();
-                    if (row0 < p.M) {
-#pragma unroll 1
-                        for (int c = 0; c < kChunks; ++c) {
-                            const int ccol = col0 + c * kChunkCols;
-                            if (ccol >= p.N) break;
-                            uint32_t own[32];
-                            tmem_ld_32x32b_x32(t_row + c * kChunkCols, own);
-                            tmem_ld_wait(own);
-                            float acc[32];
-                            for (int k = 0; k < w.ncontrib; ++k) {   // contributor order: fixed sum order
-                                float part[32];
-                                if (k == w.contrib) {
+            } else {
+                // First piece of a split tile, the last item of this unit: its
+                // operand ring is idle now that the accumulator is full.  Wait
+                // for the other piece's partial, pull it into this warp's
+                // 32 KB of the ring with one bulk copy, and store own + other
+                // (two addends: the fp32 sum is the same in either order).
+                int* flag = p.flags + (w.sk_index * kCluster + (int)crank) * 4 + quad;
+                const uint32_t fix = base + (uint32_t)(warp - 2) * (uint32_t)kFixupBytes;
+                const uint32_t fbar = fix_bar(warp - 2);
+                bool ok = wait_flag_bounded(flag, abort_flag, p, 6, w.sk_index);
+                if (ok) {
+                    if (lane == 0) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(fbar, C::kPartialBytes);
+                        bulk_copy_g2s(fix, p.partials + ((size_t)(w.slot * kCluster + (int)crank) * 4 + quad) * kPartialFloats,
+                                      C::kPartialBytes, fbar);
+                    }
+                    ok = __all_sync(0xffffffffu, wait_bounded<false>(fbar, 0, abort_flag, p, 7, w.sk_index));
+                }
+                if (!ok) break;
+                if (row0 < p.M) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(t_row, ra);
+                    tmem_ld_wait(ra);
 #pragma unroll
-                                    for (int e = 0; e < 32; ++e) part[e] = __uint_as_float(own[e]);
-                                } else {
-                                    const float4* src = reinterpret_cast<const float4*>(
-                                        p.partials +
-                                        ((size_t)(contributor_slot(p.sched, w.sk_index, k) * kCluster + (int)crank) * 4 +
-                                         quad) * part_stride);
-#pragma unroll
-                                    for (int q = 0; q < 8; ++q) {
-                                        const float4 f = __ldcg(&src[(c * 8 + q) * 32 + lane]);
-                                        part[4 * q] = f.x;
-                                        part[4 * q + 1] = f.y;
-                                        part[4 * q + 2] = f.z;
-                                        part[4 * q + 3] = f.w;
-                                    }
-                                }
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) acc[e] = k == 0 ? part[e] : acc[e] + part[e];
-                            }
+                    for (int c = 0; c < kChunks; ++c) {
+                        uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                        uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                        if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
+                        const int ccol = col0 + c * kChunkCols;
+                        if (ccol < p.N) {
                             uint32_t sum[32];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) sum[e] = __float_as_uint(acc[e]);
+                            for (int q = 0; q < 8; ++q) {
+                                uint32_t o[4];
+                                ld_shared_v4(fix + (uint32_t)(((c * 8 + q) * 32 + lane) * 16), o[0], o[1], o[2], o[3]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    sum[4 * q + e] = __float_as_uint(__uint_as_float(cur[4 * q + e]) + __uint_as_float(o[e]));
+                            }
                             store_chunk(sum, ccol, row0);
                         }
+                        if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
-                    if (lane == 0) *counter = 0;   // ready for the next launch
-                    if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrReduceDone, i);
                 }
+                if (lane == 0) *flag = 0;   // ready for the next launch
+                if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrReduceDone, i);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -585,7 +618,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 else mbar_arrive_local(acce_bar(b));
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
+        // Only the staging buffers' reads must be done before shared memory
+        // goes away; the writes to C complete with the grid.
+        if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
         if (warp == 2 && lane == 0) GEMM_TR(kTrEpiDone);
     }

@@ -1,23 +1,38 @@
 // schedule.h -- static work schedule of the persistent GEMM: which output
 // tiles and which K ranges each resident CTA pair ("unit") processes.
 //
-// Data-parallel waves, then a stream-K tail.  With T tiles on P units,
-// W = T / P full waves run whole tiles (unit u takes tiles u, u+P, ...).
-// The R = T - W*P tiles left over would leave P - R units idle for a whole
-// tile time, so instead their R*KB k-blocks (KB per tile) are cut into P
-// contiguous ranges of near-equal length, one per unit.  A range may start
-// or end inside a tile; each piece of a tile ("segment") accumulates a
-// partial sum over its k-blocks.  Every contributor of a split tile stores
-// its fp32 partial in a workspace slot and bumps the tile's counter; the
-// last to arrive adds all partials in contributor order (a fixed order, so
-// results do not depend on timing) and writes C.
+// Whole tiles in data-parallel waves, then a stream-K part for a partial
+// last wave.  With T tiles on P units and R = T mod P > 0, plain waves would
+// leave P - R units idle for a whole tile time.  Instead the first W - 1
+// waves (W = T / P) run whole tiles and the remaining S = P + R tiles -- the
+// last full wave plus the partial one -- have their S*KB k-blocks cut into P
+// contiguous ranges of near-equal length, one per unit.  Every range is
+// longer than a tile (S > P), so a tile is split between at most two units:
+//
+//   * contributor 0 holds the tile's first k-blocks; that piece ends its
+//     unit's range, so it is the unit's last work item;
+//   * contributor 1 holds the rest; that piece starts its unit's range, so
+//     it is the unit's first stream-K item and is finished long before.
+//
+// Contributor 1 publishes its fp32 partial in a workspace slot (one slot per
+// unit: a unit starts at most one range) and raises a flag; contributor 0
+// waits for the flag, adds the partial to its own accumulator and writes C.
+// With two addends the fp32 sum does not depend on which one is "own", so
+// results are deterministic.
+//
+// With fewer tiles than units (W = 0) and T <= P/2, each tile is instead
+// split into two K halves on 2T units (same protocol, same roles).
+//
+// Stream-K is used only when it is predicted to pay: the time saved, in
+// k-blocks of one unit, must exceed kFixupKBlocks, an estimate of the
+// publish/wait/add cost of a split tile.
 //
 // Prior art: the persistent grid of "Collective matrix multiplication"
 // (grid = number of SMs, static tile loop); the split of the reduction
-// dimension across programs with an fp32 accumulator written once at the
-// end follows the K-accumulating matmul of "Chapter 7: Writing Custom
-// Kernels with Pallas", §4.1'/§4.4 (there the K steps of one block run in
-// one program; here the last contributor does the final accumulation).
+// dimension with an fp32 accumulator cast once at the end follows the
+// K-accumulating matmul of "Chapter 7: Writing Custom Kernels with Pallas",
+// §4.1'/§4.4 (there one program runs all K steps of a block; here two units
+// share them and one of them adds the two partial sums).
 //
 // Plain C++ with host/device qualifiers so the host code and the CPU tests
 // can run exactly the logic the kernel runs.
@@ -32,18 +47,27 @@
 
 namespace gb300 {
 
+// Estimated cost of a split tile's fix-up, in k-blocks of MMA time: on
+// GB300 the finishing unit's tail (bulk copy of the other partial, add,
+// store) measured ~3-4.5 µs against ~2 µs for a plain last epilogue, and the
+// units' end times spread by a few µs more; 12 k-blocks of a 256-wide tile
+// are ~3.5 µs.
+constexpr int kFixupKBlocks = 12;
+
 struct Schedule {
     int tiles;        // T: output tiles
-    int units;        // P: resident CTA pairs (or single CTAs)
+    int units;        // P: units that run (the grid)
     int kb;           // KB: k-blocks per tile
-    int dp_waves;     // W: whole tiles per unit in the data-parallel part
-    int sk_tiles;     // R: tiles whose k-blocks are spread over all units (0 = none)
+    int dp_waves;     // whole tiles per unit before the stream-K part (all of T when sk_tiles == 0)
+    int sk_tiles;     // S: tiles whose k-blocks are spread over all units (0 = none)
 };
 
 // One unit of work for every role of a unit: tile `tile`, k-blocks
-// [kb_begin, kb_end).  For a split tile, `ncontrib` > 1, `contrib` is this
-// segment's position among the tile's contributors, `slot` is this unit's
-// workspace slot for the partial, `sk_index` the tile's index in the tail.
+// [kb_begin, kb_end).  For a split tile (`ncontrib` == 2), `contrib` is 0
+// for the piece holding the tile's first k-blocks (it finishes the tile)
+// and 1 for the other, `slot` is the workspace slot of contributor 1's
+// partial (the index of its unit) and `sk_index` the tile's index in the
+// stream-K part (its flag).
 struct Work {
     int tile;
     int kb_begin, kb_end;
@@ -52,33 +76,39 @@ struct Work {
     int sk_index;
 };
 
-// Decide the split.  Stream-K is used only when the last wave is at most
-// 7/8 full and every unit gets at least two k-blocks of the tail.
 GB300_HD Schedule make_schedule(int tiles, int units, int kb, bool allow_stream_k) {
     Schedule s;
     s.tiles = tiles;
-    s.units = units;
     s.kb = kb;
-    const int rem = tiles % units;
-    const int64_t tail_work = (int64_t)rem * kb;
-    const bool split = allow_stream_k && rem != 0 && (int64_t)rem * 8 <= (int64_t)units * 7 &&
-                       tail_work >= 2 * (int64_t)units;
-    if (split) {
-        s.dp_waves = tiles / units;
-        s.sk_tiles = rem;
-    } else {
-        s.dp_waves = (tiles + units - 1) / units;
-        s.sk_tiles = 0;
+    const int waves = tiles / units, rem = tiles % units;
+    if (allow_stream_k && rem != 0 && kb >= 2) {
+        if (waves >= 1 && (int64_t)(units - rem) * kb > (int64_t)kFixupKBlocks * units) {
+            s.units = units;
+            s.dp_waves = waves - 1;
+            s.sk_tiles = units + rem;
+            return s;
+        }
+        if (waves == 0 && 2 * tiles <= units && kb > 2 * kFixupKBlocks) {
+            s.units = 2 * tiles;
+            s.dp_waves = 0;
+            s.sk_tiles = tiles;
+            return s;
+        }
     }
+    // whole tiles only, never more units than tiles
+    s.units = units < tiles ? units : tiles;
+    if (s.units < 1) s.units = 1;
+    s.dp_waves = (tiles + s.units - 1) / s.units;
+    s.sk_tiles = 0;
     return s;
 }
 
-// First tail k-block (in the concatenated tail k-block space) of unit u.
+// First stream-K k-block (in the concatenated stream-K k-block space) of unit u.
 GB300_HD int64_t sk_begin(const Schedule& s, int u) {
     return (int64_t)u * ((int64_t)s.sk_tiles * s.kb) / s.units;
 }
 
-// The unit whose tail range contains tail k-block x (0 <= x < R*KB).
+// The unit whose stream-K range contains k-block x (0 <= x < S*KB).
 GB300_HD int sk_owner(const Schedule& s, int64_t x) {
     const int64_t total = (int64_t)s.sk_tiles * s.kb;
     // largest u with floor(u*total/P) <= x  <=>  u < (x+1)*P/total
@@ -88,28 +118,13 @@ GB300_HD int sk_owner(const Schedule& s, int64_t x) {
     return (int)u;
 }
 
-// Local index (0 or 1) of tail tile q within unit u's segments: a tail
-// range is shorter than one tile, so it touches at most two tiles.
-GB300_HD int sk_local_index(const Schedule& s, int u, int q) {
-    const int first_tile = (int)(sk_begin(s, u) / s.kb);
-    return q > first_tile ? 1 : 0;
-}
-
-GB300_HD int sk_slot(int u, int local) { return 2 * u + local; }
-
-// Number of work items of unit u: its data-parallel tiles plus its tail
-// segments.
+// Number of work items of unit u: its whole tiles plus its stream-K pieces.
 GB300_HD int work_count(const Schedule& s, int u) {
-    int dp = 0;
-    if (s.sk_tiles == 0) {
-        dp = u < s.tiles ? (s.tiles - 1 - u) / s.units + 1 : 0;
-        return dp;
-    }
-    dp = s.dp_waves;
+    if (s.sk_tiles == 0) return u < s.tiles ? (s.tiles - 1 - u) / s.units + 1 : 0;
     const int64_t b0 = sk_begin(s, u), b1 = sk_begin(s, u + 1);
-    if (b1 <= b0) return dp;
+    if (b1 <= b0) return s.dp_waves;
     const int q0 = (int)(b0 / s.kb), q1 = (int)((b1 - 1) / s.kb);
-    return dp + (q1 - q0 + 1);
+    return s.dp_waves + (q1 - q0 + 1);
 }
 
 // The j-th work item of unit u (0 <= j < work_count(s, u)).
@@ -125,29 +140,21 @@ GB300_HD Work work_item(const Schedule& s, int u, int j) {
         w.sk_index = -1;
         return w;
     }
-    const int seg = j - s.dp_waves;                 // 0 or 1
     const int64_t b0 = sk_begin(s, u), b1 = sk_begin(s, u + 1);
-    const int q = (int)(b0 / s.kb) + seg;
+    const int q = (int)(b0 / s.kb) + (j - s.dp_waves);
     const int64_t tile_lo = (int64_t)q * s.kb, tile_hi = tile_lo + s.kb;
     const int64_t lo = b0 > tile_lo ? b0 : tile_lo;
     const int64_t hi = b1 < tile_hi ? b1 : tile_hi;
+    const int first = sk_owner(s, tile_lo);
+    const int last = sk_owner(s, tile_hi - 1);
     w.tile = s.dp_waves * s.units + q;
     w.kb_begin = (int)(lo - tile_lo);
     w.kb_end = (int)(hi - tile_lo);
-    const int first = sk_owner(s, tile_lo);
-    const int last = sk_owner(s, tile_hi - 1);
     w.contrib = u - first;
     w.ncontrib = last - first + 1;
-    w.slot = sk_slot(u, seg);
+    w.slot = w.ncontrib > 1 ? last : -1;
     w.sk_index = q;
     return w;
-}
-
-// Workspace slot holding contributor c's partial of tail tile q.
-GB300_HD int contributor_slot(const Schedule& s, int q, int c) {
-    const int first = sk_owner(s, (int64_t)q * s.kb);
-    const int u = first + c;
-    return sk_slot(u, sk_local_index(s, u, q));
 }
 
 }  // namespace gb300

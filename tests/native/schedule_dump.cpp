@@ -2,7 +2,7 @@
 // "tiles units kblocks allow_stream_k" lines on stdin and prints, for each,
 // the schedule and every unit's work items, so the CPU tests can check that
 // every (tile, k-block) is covered exactly once and the stream-K bookkeeping
-// (contributor order, slots, counters) is consistent.
+// (contributor roles, slots, flags) is consistent.
 #include <cstdio>
 
 #include "schedule.h"
@@ -18,9 +18,6 @@ int main() {
                 const gb300::Work w = gb300::work_item(s, u, j);
                 std::printf("W %d %d %d %d %d %d %d %d %d\n", u, j, w.tile, w.kb_begin, w.kb_end, w.contrib,
                             w.ncontrib, w.slot, w.sk_index);
-                if (w.ncontrib > 1)
-                    for (int c = 0; c < w.ncontrib; ++c)
-                        std::printf("C %d %d %d\n", w.sk_index, c, gb300::contributor_slot(s, w.sk_index, c));
             }
         }
         std::printf("E\n");

@@ -200,30 +200,35 @@ def test_tile_width_choice_fills_waves(g, plan, name, expect):
         assert launch["tile_n"] == expect, launch
 
 
-# (M, N, K, max CTAs): shapes whose last wave is split along K over all units
+# (M, N, K, tile width, {CTAs per unit: CTA cap}): shapes whose schedule
+# splits tiles along K, for every unit size
 STREAM_K_CASES = [
-    (1024, 1280, 1024, 0),   # fewer tiles than units: every tile split over ~4 units
-    (1300, 1000, 1000, 12),  # few units: full waves + split tiles
-    (520, 776, 2056, 8),     # ragged M/N/K
+    # fewer tiles than half the units: every tile halved along K
+    (1024, 1280, 2048, 256, {1: 0, 2: 0, 4: 0}),
+    # a partial last wave: the last whole wave and the rest spread over all units
+    (1300, 1096, 2000, 256, {1: 16, 2: 14, 4: 8}),
+    # the same, ragged M/N and a partial last k-block
+    (520, 776, 2056, 128, {1: 8, 2: 8, 4: 16}),
 ]
 
 
 @pytest.mark.parametrize("unit", UNITS)
-@pytest.mark.parametrize("case", STREAM_K_CASES, ids=lambda c: "x".join(map(str, c)))
-def test_stream_k_tail(g, fresh_plan, unit, case):
-    M, N, K, ctas = case
+@pytest.mark.parametrize("case", STREAM_K_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_stream_k(g, fresh_plan, unit, case):
+    M, N, K, tile_n, caps = case
     configure(g, fresh_plan, unit)
-    pair = unit
-    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, ctas)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, caps[unit])
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, tile_n)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STREAM_K, 1)
     for out in OUTS:
         # integer inputs: exact whatever the split
         A, B = draw(M, N, K, dist="int", seed=K + out)
         C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), out))
+        assert g.gemm_plan_last_launch(fresh_plan)["sk_tiles"] > 0, "the schedule did not split"
         C_ref, _ = oracle_full(A, B)
         want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
-        assert np.array_equal(C, want), f"stream-K {case} pair={pair} out={out}"
-        # random inputs: tolerance, and bitwise repeatable (fixed reduction order)
+        assert np.array_equal(C, want), f"stream-K {case} unit={unit} out={out}"
+        # random inputs: tolerance, and bitwise repeatable
         dtype = wl.F16 if out == wl.F16 else wl.BF16
         A, B = draw(M, N, K, dtype=dtype, seed=K * 7 + out)
         Ad, Bd = A.cuda(), B.cuda()
@@ -231,7 +236,7 @@ def test_stream_k_tail(g, fresh_plan, unit, case):
         C2 = run(g, fresh_plan, Ad, Bd, out)
         assert torch.equal(C1.view(torch.uint8), C2.view(torch.uint8)), "stream-K result not repeatable"
         C_ref, S = oracle_full(A, B)
-        parity.assert_within(parity.to_f64(C1), C_ref, S, out, f"stream-K {case} pair={pair} out={out}")
+        parity.assert_within(parity.to_f64(C1), C_ref, S, out, f"stream-K {case} unit={unit} out={out}")
 
 
 def test_stream_k_off_matches_within_tolerance(g, fresh_plan):

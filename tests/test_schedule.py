@@ -4,10 +4,12 @@ The same header the kernel compiles is built here with g++ into a small
 driver that prints every unit's work items.  For many (tiles, units,
 k-blocks) combinations, including the benchmark shapes on 76 CTA pairs, the
 tests check that every (tile, k-block) is computed exactly once, that the
-data-parallel part is balanced and the stream-K tail splits its k-blocks
-evenly, and that the split-tile bookkeeping the epilogue relies on
-(contributor order, contributor count, workspace slots, counters) is
-consistent.
+whole-tile waves are balanced and the stream-K part splits its k-blocks
+evenly, and the invariants the epilogue's fix-up relies on: a tile has at
+most two pieces; the piece with the tile's first k-blocks is its unit's last
+work item and finishes the tile; the other is its unit's first stream-K
+item; both name the same workspace slot (the second piece's unit) and the
+same flag; no slot or flag is used twice in a launch.
 """
 import os
 import subprocess
@@ -19,6 +21,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300", "csrc")
 SRC = os.path.join(ROOT, "tests", "native", "schedule_dump.cpp")
+FIXUP_KBLOCKS = 12  # kFixupKBlocks in schedule.h
 
 
 @pytest.fixture(scope="module")
@@ -33,63 +36,84 @@ def dump(tmp_path_factory):
         for line in out.splitlines():
             f = line.split()
             if f[0] == "S":
-                cur = {"sched": tuple(map(int, f[1:])), "work": [], "contrib_slots": {}}
+                cur = {"sched": tuple(map(int, f[1:])), "work": []}
             elif f[0] == "W":
                 cur["work"].append(tuple(map(int, f[1:])))
-            elif f[0] == "C":
-                q, c, slot = map(int, f[1:])
-                cur["contrib_slots"][(q, c)] = slot
             elif f[0] == "E":
                 results.append(cur)
         return results
     return run
 
 
+def expected_mode(T, P, KB, allow):
+    """Which schedule the rule in schedule.h picks: 'dp', 'wave' or 'halves'."""
+    W, R = divmod(T, P)
+    if allow and R and KB >= 2:
+        if W >= 1 and (P - R) * KB > FIXUP_KBLOCKS * P:
+            return "wave"
+        if W == 0 and 2 * T <= P and KB > 2 * FIXUP_KBLOCKS:
+            return "halves"
+    return "dp"
+
+
 def check(res, tiles, units, kb, allow):
-    T, P, KB, W, R = res["sched"]
-    assert (T, P, KB) == (tiles, units, kb)
+    T, P, KB, W, S = res["sched"]
+    assert (T, KB) == (tiles, kb)
+    mode = expected_mode(tiles, units, kb, allow)
+    if mode == "dp":
+        assert S == 0 and P == max(1, min(units, tiles)) and W == -(-T // P)
+    elif mode == "wave":
+        assert P == units and W == tiles // units - 1 and S == units + tiles % units
+    else:
+        assert P == 2 * tiles and W == 0 and S == tiles
     cover = defaultdict(int)
-    per_unit_kblocks = defaultdict(int)
-    tile_contribs = defaultdict(list)
-    slots_used = set()
+    per_unit_sk = defaultdict(int)
+    items = defaultdict(list)
+    pieces = defaultdict(list)
     for (u, j, tile, kb0, kb1, c, n, slot, q) in res["work"]:
         assert 0 <= u < P and 0 <= tile < T and 0 <= kb0 < kb1 <= KB
+        items[u].append(j)
         for k in range(kb0, kb1):
             cover[(tile, k)] += 1
-        per_unit_kblocks[u] += kb1 - kb0
+        if j >= W and S:
+            per_unit_sk[u] += kb1 - kb0
+            assert tile == W * P + q
         if n == 1:
-            assert (kb0, kb1) == (0, KB), "an unsplit tile must cover all of K"
+            assert (kb0, kb1) == (0, KB) and slot == -1, "an unsplit tile must cover all of K"
         else:
-            assert R > 0 and tile >= W * P and q == tile - W * P
-            assert slot in (2 * u, 2 * u + 1)
-            assert slot not in slots_used, "a workspace slot is reused within a launch"
-            slots_used.add(slot)
-            tile_contribs[tile].append((c, n, kb0, u, slot))
+            assert n == 2 and S > 0 and c in (0, 1)
+            pieces[tile].append((c, u, j, kb0, kb1, slot, q))
     # every (tile, k-block) exactly once
     assert len(cover) == T * KB and set(cover.values()) == {1}
-    # split tiles: contributors 0..n-1 in k order, slots found by contributor_slot
-    for tile, lst in tile_contribs.items():
+    last_item = {u: max(js) for u, js in items.items()}
+    slots, flags = set(), set()
+    for tile, lst in pieces.items():
         lst.sort()
-        n = lst[0][1]
-        assert [c for c, *_ in lst] == list(range(n)) and all(x[1] == n for x in lst)
-        assert [kb0 for _, _, kb0, _, _ in lst] == sorted(kb0 for _, _, kb0, _, _ in lst)
-        q = tile - W * P
-        for c, _, _, u, slot in lst:
-            assert res["contrib_slots"][(q, c)] == slot
-    if R == 0:
-        assert W == -(-T // P)
-        loads = [per_unit_kblocks[u] for u in range(P)]
-        assert max(loads) - min(loads) <= KB
+        assert [c for c, *_ in lst] == [0, 1], lst
+        (_, u0, j0, a0, b0, s0, q0), (_, u1, j1, a1, b1, s1, q1) = lst
+        assert a0 == 0 and b0 == a1 and b1 == KB, "the two pieces split K at one point"
+        assert j0 == last_item[u0], "the finishing piece is its unit's last item"
+        assert j1 == W, "the other piece is its unit's first stream-K item"
+        assert s0 == s1 == u1 and q0 == q1
+        assert s1 not in slots and q1 not in flags
+        slots.add(s1)
+        flags.add(q1)
+        assert 0 <= q1 < 2 * P
+    if S:
+        loads = [per_unit_sk[u] for u in range(P)]
+        assert max(loads) - min(loads) <= 1, loads
+        if mode == "wave":
+            assert min(loads) >= KB, "every stream-K range is longer than a tile"
     else:
-        assert allow and W == T // P and R == T - W * P and R * 8 <= P * 7
-        tail = [per_unit_kblocks[u] - W * KB for u in range(P)]
-        assert max(tail) - min(tail) <= 1 and min(tail) >= 2, tail
+        loads = [len(items[u]) for u in range(P)]
+        assert max(loads) - min(loads) <= 1
 
 
 BENCH_CASES = [
-    (256, 76, 64, True),     # bf16 4096^3, 256x256 tiles on 76 pairs
-    (64, 76, 64, True),      # f16 1024x4096x4096: fewer tiles than pairs
-    (192, 76, 79, True),     # ragged 4000x3000x5000 (K tail block)
+    (304, 76, 64, True),     # bf16 4096^3, 256x224 tiles on 76 pairs: 4 whole waves
+    (256, 76, 64, True),     # bf16 4096^3, 256x256 tiles: 3.4 waves
+    (76, 76, 64, True),      # f16 1024x4096x4096, 256x224 tiles: one whole wave
+    (96, 36, 79, True),      # ragged 4000x3000x5000 on 36 four-CTA clusters (K tail block)
     (1024, 76, 128, True),   # bf16 8192^3
     (1, 76, 4, True),        # 256^3
     (256, 76, 64, False),
@@ -103,17 +127,22 @@ def test_benchmark_shapes(dump):
 
 
 def test_expected_splits(dump):
-    res = dump([(256, 76, 64, True), (64, 76, 64, True), (1, 76, 4, True), (76, 76, 64, True)])
-    assert res[0]["sched"][3:] == (3, 28)    # 3 full waves + 28 tiles spread over all pairs
-    assert res[1]["sched"][3:] == (0, 64)    # all 64 tiles spread over 76 pairs
-    assert res[2]["sched"][3:] == (1, 0)     # too little work to split
-    assert res[3]["sched"][3:] == (1, 0)     # exactly one full wave
+    res = dump([(256, 76, 64, True), (1024, 76, 128, True), (20, 76, 32, True), (1, 76, 4, True),
+                (76, 76, 64, True), (150, 76, 64, True), (40, 76, 64, True), (144, 76, 48, True)])
+    assert res[0]["sched"][1:] == (76, 64, 2, 104)   # 2 whole waves + 76 + 28 tiles spread over all pairs
+    assert res[1]["sched"][1:] == (76, 128, 12, 112)  # 8192^3: 12 whole waves + 112 tiles spread
+    assert res[2]["sched"][1:] == (40, 32, 0, 20)    # 20 tiles halved over 40 units
+    assert res[3]["sched"][1:] == (1, 4, 1, 0)       # too little K to split
+    assert res[4]["sched"][1:] == (76, 64, 1, 0)     # exactly one whole wave
+    assert res[5]["sched"][1:] == (76, 64, 2, 0)     # 74 of 76 in the last wave: splitting would not pay
+    assert res[6]["sched"][1:] == (40, 64, 1, 0)     # more than half the units: whole tiles
+    assert res[7]["sched"][1:] == (76, 48, 2, 0)     # 3072^3: 68 of 76 in the last wave, short K
 
 
 def test_random_shapes(dump):
     rng = np.random.default_rng(0)
     cases = []
-    for _ in range(400):
+    for _ in range(600):
         P = int(rng.integers(1, 160))
         T = int(rng.integers(1, 6 * P + 3))
         KB = int(rng.integers(1, 200))
