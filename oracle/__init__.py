@@ -22,7 +22,8 @@ _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "libgemm_oracle.so")
 _lock = threading.Lock()
 
-BF16, F16, F32 = 0, 1, 2
+BF16, F16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+FP8 = (E4M3, E5M2)
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
@@ -54,11 +55,17 @@ def _bind(path: str):
     lib.oracle_decode16_array.argtypes = [u16p, dp, ctypes.c_int64, ctypes.c_int]
     lib.oracle_encode16_array.restype = None
     lib.oracle_encode16_array.argtypes = [dp, u16p, ctypes.c_int64, ctypes.c_int]
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_decode8.restype = ctypes.c_double
+    lib.oracle_decode8.argtypes = [ctypes.c_uint8, ctypes.c_int]
+    lib.oracle_decode8_array.restype = None
+    lib.oracle_decode8_array.argtypes = [u8p, dp, ctypes.c_int64, ctypes.c_int]
+    vp = ctypes.c_void_p
     lib.oracle_gemm.restype = ctypes.c_int
-    lib.oracle_gemm.argtypes = [u16p, u16p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+    lib.oracle_gemm.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                 ctypes.c_int64, dp, dp, ctypes.c_int]
     lib.oracle_gemm_entries.restype = ctypes.c_int
-    lib.oracle_gemm_entries.argtypes = [u16p, u16p, ctypes.c_int, ctypes.c_int64,
+    lib.oracle_gemm_entries.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int64, i64p, i64p,
                                         ctypes.c_int64, dp, dp, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -70,6 +77,15 @@ def _u16(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x)
     if x.dtype != np.uint16:
         raise TypeError("expected the raw 16-bit patterns as a uint16 array")
+    return x
+
+
+def _in_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Input patterns: uint16 for bf16/f16, uint8 for the fp8 formats."""
+    x = np.ascontiguousarray(x)
+    want = np.uint8 if dtype in FP8 else np.uint16
+    if x.dtype != want:
+        raise TypeError(f"expected the raw bit patterns as a {np.dtype(want).name} array for dtype {dtype}")
     return x
 
 
@@ -85,11 +101,15 @@ class Oracle:
         self.lib = _bind(path)
 
     def decode(self, bits: np.ndarray, dtype: int) -> np.ndarray:
-        """Exact float64 values of bf16 (dtype 0) or f16 (dtype 1) bit patterns."""
-        bits = _u16(bits)
+        """Exact float64 values of bf16 (0), f16 (1), E4M3 (3) or E5M2 (4) bit patterns."""
+        bits = _in_bits(bits, dtype)
         out = np.empty(bits.shape, dtype=np.float64)
-        self.lib.oracle_decode16_array(_ptr(bits, ctypes.c_uint16), _ptr(out, ctypes.c_double),
-                                       bits.size, dtype)
+        if dtype in FP8:
+            self.lib.oracle_decode8_array(_ptr(bits, ctypes.c_uint8), _ptr(out, ctypes.c_double),
+                                          bits.size, dtype)
+        else:
+            self.lib.oracle_decode16_array(_ptr(bits, ctypes.c_uint16), _ptr(out, ctypes.c_double),
+                                           bits.size, dtype)
         return out
 
     def encode(self, x: np.ndarray, dtype: int) -> np.ndarray:
@@ -103,14 +123,14 @@ class Oracle:
     def gemm(self, A_bits: np.ndarray, B_bits: np.ndarray, dtype: int, threads: int = 0
              ) -> Tuple[np.ndarray, np.ndarray]:
         """C = A·Bᵀ and S = |A|·|B|ᵀ in float64.  A: [M,K], B: [N,K] bit patterns."""
-        A_bits, B_bits = _u16(A_bits), _u16(B_bits)
+        A_bits, B_bits = _in_bits(A_bits, dtype), _in_bits(B_bits, dtype)
         if A_bits.ndim != 2 or B_bits.ndim != 2 or A_bits.shape[1] != B_bits.shape[1]:
             raise ValueError("A must be [M,K] and B [N,K]")
         M, K = A_bits.shape
         N = B_bits.shape[0]
         C = np.zeros((M, N), dtype=np.float64)
         S = np.zeros((M, N), dtype=np.float64)
-        rc = self.lib.oracle_gemm(_ptr(A_bits, ctypes.c_uint16), _ptr(B_bits, ctypes.c_uint16),
+        rc = self.lib.oracle_gemm(A_bits.ctypes.data, B_bits.ctypes.data,
                                   dtype, M, N, K, _ptr(C, ctypes.c_double),
                                   _ptr(S, ctypes.c_double), threads)
         if rc != 0:
@@ -120,7 +140,7 @@ class Oracle:
     def gemm_entries(self, A_bits: np.ndarray, B_bits: np.ndarray, dtype: int, I: np.ndarray,
                      J: np.ndarray, threads: int = 0) -> Tuple[np.ndarray, np.ndarray]:
         """C[I[t], J[t]] and S[I[t], J[t]] only, for sampled checks of large outputs."""
-        A_bits, B_bits = _u16(A_bits), _u16(B_bits)
+        A_bits, B_bits = _in_bits(A_bits, dtype), _in_bits(B_bits, dtype)
         M, K = A_bits.shape
         N = B_bits.shape[0]
         I = np.ascontiguousarray(I, dtype=np.int64)
@@ -129,8 +149,7 @@ class Oracle:
             raise ValueError("I and J must have the same shape")
         C = np.zeros(I.shape, dtype=np.float64)
         S = np.zeros(I.shape, dtype=np.float64)
-        rc = self.lib.oracle_gemm_entries(_ptr(A_bits, ctypes.c_uint16),
-                                          _ptr(B_bits, ctypes.c_uint16), dtype, M, N, K,
+        rc = self.lib.oracle_gemm_entries(A_bits.ctypes.data, B_bits.ctypes.data, dtype, M, N, K,
                                           _ptr(I, ctypes.c_int64), _ptr(J, ctypes.c_int64),
                                           I.size, _ptr(C, ctypes.c_double),
                                           _ptr(S, ctypes.c_double), threads)

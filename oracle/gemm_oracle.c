@@ -19,9 +19,13 @@
  * over K written out in "Chapter 7: Writing Custom Kernels with Pallas",
  * §4.1.  The pages check their kernels against a float64 reference
  * (Chapter 7, §0 "common preparation" and §2.3); this oracle does the same.
- * a(i,k), b(j,k) are the exact values of the bf16/f16 inputs; every product
- * of two such values is exact in double, and the K-sum is evaluated
- * sequentially in k.  S is the sum of magnitudes used by the error bound.
+ * a(i,k), b(j,k) are the exact values of the inputs -- bf16 or f16, or one
+ * of the two 8-bit float formats the pages list among the tensor-core
+ * operand types ("Writing Mosaic GPU kernels with Pallas", "Blackwell
+ * (tcgen05)", "Issuing the operation": float8_e5m2 and float8_e4m3fn).
+ * Every product of two such values is exact in double, and the K-sum is
+ * evaluated sequentially in k.  S is the sum of magnitudes used by the
+ * error bound.
  *
  * Rows i are spread over OpenMP threads; nothing else is blocked or reordered.
  */
@@ -33,7 +37,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_BF16 = 0, ORACLE_F16 = 1, ORACLE_F32 = 2 };
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
 
 /* Field widths of the two 16-bit formats.
  *   bf16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits -- the
@@ -103,22 +107,64 @@ void oracle_decode16_array(const uint16_t* bits, double* out, int64_t n, int dty
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_decode16(bits[i], dtype);
 }
 
+/* Exact value of an 8-bit float pattern (sign in bit 7).
+ *   E5M2: 5 exponent bits (bias 15), 2 fraction bits, with the IEEE-754
+ *         meaning of every field: the all-ones exponent holds the
+ *         infinities (fraction 0) and NaNs.
+ *   E4M3 (the "fn" variant: finite numbers only): 4 exponent bits (bias 7),
+ *         3 fraction bits; no infinities, and the all-ones exponent still
+ *         holds normal numbers (up to 448) except S.1111.111, its only NaN. */
+double oracle_decode8(uint8_t bits, int dtype) {
+    const int eb = dtype == ORACLE_E4M3 ? 4 : 5, fb = dtype == ORACLE_E4M3 ? 3 : 2;
+    const int bias8 = (1 << (eb - 1)) - 1;
+    const int sign8 = (bits >> 7) & 1;
+    const int e = (bits >> fb) & ((1 << eb) - 1);
+    const uint32_t f = bits & ((1u << fb) - 1);
+    double v;
+    if (dtype == ORACLE_E4M3 && e == 15 && f == 7) {
+        v = NAN;
+    } else if (dtype == ORACLE_E5M2 && e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, 1 - bias8 - fb);                 /* subnormal or zero */
+    } else {
+        v = ldexp((double)((1u << fb) | f), e - bias8 - fb);  /* normal */
+    }
+    return sign8 ? -v : v;
+}
+
+void oracle_decode8_array(const uint8_t* bits, double* out, int64_t n, int dtype) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_decode8(bits[i], dtype);
+}
+
+static int is_input_dtype(int dtype) {
+    return dtype == ORACLE_BF16 || dtype == ORACLE_F16 || dtype == ORACLE_E4M3 || dtype == ORACLE_E5M2;
+}
+
+/* Value of element `idx` of an input array stored in `dtype` (16-bit
+ * patterns for bf16/f16, 8-bit patterns for the fp8 formats). */
+static double input_value(const void* bits, int64_t idx, int dtype) {
+    if (dtype == ORACLE_BF16 || dtype == ORACLE_F16) return oracle_decode16(((const uint16_t*)bits)[idx], dtype);
+    return oracle_decode8(((const uint8_t*)bits)[idx], dtype);
+}
+
 void oracle_encode16_array(const double* x, uint16_t* out, int64_t n, int dtype) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_encode16(x[i], dtype);
 }
 
-/* Full product.  A: M×K bit patterns, B: N×K bit patterns, both in `dtype`.
- * C and S: M×N doubles (S may be NULL).  Returns 0, or -1 on bad arguments
- * or when memory for the decoded operands cannot be had. */
-int oracle_gemm(const uint16_t* A, const uint16_t* B, int dtype, int64_t M, int64_t N, int64_t K,
+/* Full product.  A: M×K bit patterns, B: N×K bit patterns, both in `dtype`
+ * (uint16 elements for bf16/f16, uint8 for E4M3/E5M2).  C and S: M×N
+ * doubles (S may be NULL).  Returns 0, or -1 on bad arguments or when memory
+ * for the decoded operands cannot be had. */
+int oracle_gemm(const void* A, const void* B, int dtype, int64_t M, int64_t N, int64_t K,
                 double* C, double* S, int nthreads) {
-    if (M < 0 || N < 0 || K < 0 || (dtype != ORACLE_BF16 && dtype != ORACLE_F16)) return -1;
+    if (M < 0 || N < 0 || K < 0 || !is_input_dtype(dtype)) return -1;
     if (M == 0 || N == 0) return 0;
     double* a = (double*)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
     double* b = (double*)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
     if (!a || !b) { free(a); free(b); return -1; }
-    oracle_decode16_array(A, a, M * K, dtype);
-    oracle_decode16_array(B, b, N * K, dtype);
+    for (int64_t t = 0; t < M * K; ++t) a[t] = input_value(A, t, dtype);
+    for (int64_t t = 0; t < N * K; ++t) b[t] = input_value(B, t, dtype);
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #else
@@ -147,9 +193,9 @@ int oracle_gemm(const uint16_t* A, const uint16_t* B, int dtype, int64_t M, int6
 /* Selected entries only: C[t] = sum_k a(I[t],k)·b(J[t],k), for t < n.  Used
  * to check full-size outputs at sampled positions.  Same arithmetic, same
  * order as oracle_gemm. */
-int oracle_gemm_entries(const uint16_t* A, const uint16_t* B, int dtype, int64_t M, int64_t N, int64_t K,
+int oracle_gemm_entries(const void* A, const void* B, int dtype, int64_t M, int64_t N, int64_t K,
                         const int64_t* I, const int64_t* J, int64_t n, double* C, double* S, int nthreads) {
-    if (M < 0 || N < 0 || K < 0 || (dtype != ORACLE_BF16 && dtype != ORACLE_F16)) return -1;
+    if (M < 0 || N < 0 || K < 0 || !is_input_dtype(dtype)) return -1;
     for (int64_t t = 0; t < n; ++t)
         if (I[t] < 0 || I[t] >= M || J[t] < 0 || J[t] >= N) return -1;
 #ifdef _OPENMP
@@ -159,11 +205,10 @@ int oracle_gemm_entries(const uint16_t* A, const uint16_t* B, int dtype, int64_t
 #endif
 #pragma omp parallel for schedule(dynamic, 16)
     for (int64_t t = 0; t < n; ++t) {
-        const uint16_t* ai = A + I[t] * K;
-        const uint16_t* bj = B + J[t] * K;
+        const int64_t ra = I[t] * K, rb = J[t] * K;   /* first elements of row I[t] of A, row J[t] of B */
         double acc = 0.0, mag = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            const double p = oracle_decode16(ai[k], dtype) * oracle_decode16(bj[k], dtype);
+            const double p = input_value(A, ra + k, dtype) * input_value(B, rb + k, dtype);
             acc += p;
             mag += fabs(p);
         }

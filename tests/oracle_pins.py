@@ -9,11 +9,16 @@ What pins what:
   * decode/encode of the 16-bit formats: a hand-derived bit-pattern table
     (tests/golden), every one of the 65536 patterns against numpy's binary16
     and torch's bfloat16, and rounding against those libraries' conversions.
+  * decode of the 8-bit float formats (E4M3 "fn" and E5M2): a hand-derived
+    table (tests/golden) and every one of the 256 patterns of each against
+    torch's float8 types.
   * the product: a hand-worked example (tests/golden), closed forms (identity,
     all-ones, rank-1 outer products with distinct factors), exact rational
     brute force on every shape up to 4×4×4, numpy float64 matmul within the
     float64 summation bound, symmetry C(B,A) = C(A,B)ᵀ, power-of-two
-    scaling, IEEE special values, and empty sizes.
+    scaling, IEEE special values, and empty sizes; for fp8 inputs, exact
+    rational brute force, agreement with the bf16 path on values both
+    formats hold, and sampled entries against the exact sum.
 """
 from __future__ import annotations
 
@@ -23,7 +28,8 @@ from fractions import Fraction
 import numpy as np
 import torch
 
-BF16, F16 = 0, 1
+BF16, F16, E4M3, E5M2 = 0, 1, 3, 4
+FP8_TORCH = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
@@ -36,6 +42,23 @@ def _bits_of(x: np.ndarray, dtype: int) -> np.ndarray:
 
 def _rand_bits(rng: np.random.Generator, shape, dtype: int, scale: float = 1.0) -> np.ndarray:
     return _bits_of(rng.standard_normal(shape) * scale, dtype)
+
+
+def _fp8_bits_of(x: np.ndarray, dtype: int) -> np.ndarray:
+    """fp8 patterns of values (library cast, round to nearest even)."""
+    t = torch.tensor(np.asarray(x, dtype=np.float32), dtype=torch.float32).to(FP8_TORCH[dtype])
+    return t.view(torch.uint8).numpy().copy()
+
+
+def _fp8_finite_random(rng: np.random.Generator, shape, dtype: int) -> np.ndarray:
+    """Uniformly random finite fp8 patterns: every exponent, subnormals and zeros included."""
+    bits = rng.integers(0, 256, size=shape, dtype=np.int64).astype(np.uint8)
+    if dtype == E4M3:
+        bad = (bits & 0x7F) == 0x7F
+    else:
+        bad = (bits & 0x7C) == 0x7C
+    bits[bad] = 0x00
+    return bits
 
 
 # ---------------------------------------------------------------- formats
@@ -74,6 +97,36 @@ def pin_decode_all_bf16_vs_torch(o):
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], want[~nan])
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def pin_decode_fp8_golden(o):
+    path = os.path.join(GOLDEN, "float8_bits.txt")
+    n = 0
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, hexbits, value = line.split()[:3]
+        dt = E4M3 if name == "e4m3" else E5M2
+        got = o.decode(np.array([int(hexbits, 16)], dtype=np.uint8), dt)[0]
+        want = float(value)
+        if np.isnan(want):
+            assert np.isnan(got), (name, hexbits, got)
+        else:
+            assert got == want and np.signbit(got) == np.signbit(want), (name, hexbits, got, want)
+        n += 1
+    assert n >= 20
+
+
+def pin_decode_all_fp8_vs_torch(o):
+    bits = np.arange(256, dtype=np.uint32).astype(np.uint8)
+    for dt, tdt in FP8_TORCH.items():
+        got = o.decode(bits, dt)
+        want = torch.from_numpy(bits.copy()).view(tdt).to(torch.float64).numpy()
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan), dt
+        assert np.array_equal(got[~nan], want[~nan]), dt
+        assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan])), dt
 
 
 def _encode_probe_values(rng, dtype):
@@ -266,9 +319,71 @@ def pin_entries_agree(o):
         assert S[t] >= abs(C[t])
 
 
+def pin_fp8_bruteforce(o):
+    # Every shape 1..4 in M, N, K on random finite fp8 patterns (all exponents,
+    # subnormals): the oracle is within the sequential fp64 summation bound of
+    # the exact rational sum, and S is the exact magnitude sum rounded within
+    # the same bound.  On values cast from N(0,1) (a narrow exponent range) the
+    # fp64 sums are exact and must match the rational sum exactly.
+    rng = np.random.default_rng(11)
+    for dt in (E4M3, E5M2):
+        for M in range(1, 5):
+            for N in range(1, 5):
+                for K in range(1, 5):
+                    for gen in ("wide", "narrow"):
+                        if gen == "wide":
+                            A, B = _fp8_finite_random(rng, (M, K), dt), _fp8_finite_random(rng, (N, K), dt)
+                        else:
+                            A = _fp8_bits_of(rng.standard_normal((M, K)), dt)
+                            B = _fp8_bits_of(rng.standard_normal((N, K)), dt)
+                        a, b = o.decode(A, dt), o.decode(B, dt)
+                        C, S = o.gemm(A, B, dt)
+                        for i in range(M):
+                            for j in range(N):
+                                prods = [Fraction(a[i, k]) * Fraction(b[j, k]) for k in range(K)]
+                                exact, mag = sum(prods, Fraction(0)), sum((abs(p) for p in prods), Fraction(0))
+                                if gen == "narrow":
+                                    assert C[i, j] == float(exact) and S[i, j] == float(mag), (dt, M, N, K)
+                                else:
+                                    bound = 2.0 * K * 2.0 ** -53 * float(mag)
+                                    assert abs(C[i, j] - float(exact)) <= bound, (dt, M, N, K, i, j)
+                                    assert abs(S[i, j] - float(mag)) <= bound, (dt, M, N, K, i, j)
+
+
+def pin_fp8_matches_bf16_on_shared_values(o):
+    # Values held exactly by both fp8 formats and by bf16 (small integers and
+    # halves): the same sums whichever format carries them.
+    rng = np.random.default_rng(12)
+    x = rng.integers(-8, 9, size=(23, 45)) / 2.0
+    y = rng.integers(-8, 9, size=(17, 45)) / 2.0
+    C16, S16 = o.gemm(_bits_of(x, BF16), _bits_of(y, BF16), BF16)
+    for dt in (E4M3, E5M2):
+        C8, S8 = o.gemm(_fp8_bits_of(x, dt), _fp8_bits_of(y, dt), dt)
+        assert np.array_equal(C8, C16) and np.array_equal(S8, S16), dt
+        assert np.array_equal(C8, x @ y.T)
+
+
+def pin_fp8_entries_agree(o):
+    rng = np.random.default_rng(13)
+    M, N, K = 29, 31, 41
+    for dt in (E4M3, E5M2):
+        A = _fp8_bits_of(rng.standard_normal((M, K)), dt)
+        B = _fp8_bits_of(rng.standard_normal((N, K)), dt)
+        I = rng.integers(0, M, 50)
+        J = rng.integers(0, N, 50)
+        C, S = o.gemm_entries(A, B, dt, I, J)
+        a, b = o.decode(A, dt), o.decode(B, dt)
+        for t in range(50):
+            exact = sum((Fraction(a[I[t], k]) * Fraction(b[J[t], k]) for k in range(K)), Fraction(0))
+            assert C[t] == float(exact), (dt, t)
+            assert S[t] >= abs(C[t])
+
+
 ALL_PINS = [
     pin_decode_golden, pin_decode_all_f16_vs_numpy, pin_decode_all_bf16_vs_torch,
     pin_encode_vs_numpy_f16, pin_encode_vs_torch_bf16, pin_worked_example, pin_identity,
     pin_all_ones, pin_rank1, pin_bruteforce_exact, pin_numpy_float64, pin_swap_symmetry,
     pin_power_of_two_scaling, pin_special_values, pin_empty_sizes, pin_entries_agree,
+    pin_decode_fp8_golden, pin_decode_all_fp8_vs_torch, pin_fp8_bruteforce,
+    pin_fp8_matches_bf16_on_shared_values, pin_fp8_entries_agree,
 ]

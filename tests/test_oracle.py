@@ -4,7 +4,8 @@ No GPU.  Each planted mistake is a textual change to a private copy of
 oracle/gemm_oracle.c (the oracle itself is never modified): a dropped term, a
 transposed operand, wrong signs, an off-by-one exponent bias, a broken
 subnormal scale, ties rounded away from even, a wrong row stride, a missing
-absolute value, a wrong sampled index.  Every one must fail at least one pin.
+absolute value, a wrong sampled index, and in the 8-bit decoder a
+wrong special-value rule, bias, field widths, subnormal scale or format.  Every one must fail at least one pin.
 """
 import os
 import shutil
@@ -43,8 +44,16 @@ MUTANTS = [
     ("wrong row stride of A", "const double* ai = a + i * K;", "const double* ai = a + i;"),
     ("magnitude sum without abs", "                mag += fabs(p);\n            }\n            C[i * N + j]",
      "                mag += p;\n            }\n            C[i * N + j]"),
-    ("sampled entries swap row and column", "const uint16_t* ai = A + I[t] * K;\n        const uint16_t* bj = B + J[t] * K;",
-     "const uint16_t* ai = A + (J[t] < M ? J[t] : I[t]) * K;\n        const uint16_t* bj = B + (I[t] < N ? I[t] : J[t]) * K;"),
+    ("sampled entries swap row and column", "const int64_t ra = I[t] * K, rb = J[t] * K;",
+     "const int64_t ra = (J[t] < M ? J[t] : I[t]) * K, rb = (I[t] < N ? I[t] : J[t]) * K;"),
+    ("E4M3 all-ones exponent read as infinity", "if (dtype == ORACLE_E4M3 && e == 15 && f == 7) {\n        v = NAN;",
+     "if (dtype == ORACLE_E4M3 && e == 15) {\n        v = (f == 0) ? INFINITY : NAN;"),
+    ("fp8 exponent bias off by one", "const int bias8 = (1 << (eb - 1)) - 1;", "const int bias8 = (1 << (eb - 1));"),
+    ("E5M2 read with E4M3 field widths", "const int eb = dtype == ORACLE_E4M3 ? 4 : 5, fb = dtype == ORACLE_E4M3 ? 3 : 2;",
+     "const int eb = 4, fb = 3;"),
+    ("fp8 subnormal scale off by one", "v = ldexp((double)f, 1 - bias8 - fb);", "v = ldexp((double)f, -bias8 - fb);"),
+    ("fp8 bytes decoded as f16 patterns", "return oracle_decode8(((const uint8_t*)bits)[idx], dtype);",
+     "return oracle_decode16((uint16_t)((const uint8_t*)bits)[idx], ORACLE_F16);"),
     ("overflow saturates instead of going to infinity",
      "if (e_field >= emax_field) return sign | (uint16_t)((uint32_t)emax_field << fb);  /* overflow */",
      "if (e_field >= emax_field) return sign | (uint16_t)(((uint32_t)(emax_field - 1) << fb) | ((1u << fb) - 1));"),
