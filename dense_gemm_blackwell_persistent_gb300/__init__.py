@@ -17,7 +17,7 @@ from typing import Optional
 
 from . import _build
 
-GEMM_BF16, GEMM_F16, GEMM_F32 = 0, 1, 2
+GEMM_BF16, GEMM_F16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = -1
 GEMM_ERR_UNSUPPORTED = -2
@@ -167,16 +167,19 @@ def raw_status(fn_name: str, *args) -> int:
 
 def _dtype_code(t) -> int:
     import torch
-    codes = {torch.bfloat16: GEMM_BF16, torch.float16: GEMM_F16, torch.float32: GEMM_F32}
+    codes = {torch.bfloat16: GEMM_BF16, torch.float16: GEMM_F16, torch.float32: GEMM_F32,
+             torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}
     if t not in codes:
         raise TypeError(f"unsupported dtype {t}")
     return codes[t]
 
 
 def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None):
-    """C = A @ B.T for CUDA tensors A [M,K], B [N,K] (bf16 or f16, contiguous).
+    """C = A @ B.T for CUDA tensors A [M,K], B [N,K] (contiguous; bf16, f16,
+    float8_e4m3fn or float8_e5m2, both the same).
 
-    out_dtype: torch.float32, torch.bfloat16 or torch.float16 (default: A's dtype).
+    out_dtype: torch.float32, torch.bfloat16 or torch.float16 (default: A's
+    dtype for 16-bit inputs, bf16 for fp8 inputs).
     Runs on torch's current stream of A's device.
     """
     import torch
@@ -186,7 +189,8 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None):
         raise TypeError("A and B must have the same dtype")
     if not (A.is_contiguous() and B.is_contiguous()):
         raise ValueError("A and B must be contiguous row-major")
-    out_dtype = A.dtype if out_dtype is None else out_dtype
+    if out_dtype is None:
+        out_dtype = A.dtype if A.element_size() == 2 else torch.bfloat16
     M, K = A.shape
     N = B.shape[0]
     if out is None:

@@ -1,8 +1,8 @@
 """Build the CUDA library in-tree with nvcc (sm_103a only).
 
 Produces ``dense_gemm_blackwell_persistent_gb300/_lib/libgb300gemm.so`` from
-``csrc/gemm_api.cu`` (host side) and nine objects of ``csrc/kernels_inst.cu``
-(one per unit size × output type), compiled in parallel.  The CUDA
+``csrc/gemm_api.cu`` (host side) and eighteen objects of ``csrc/kernels_inst.cu``
+(one per unit size × output type × operand width), compiled in parallel.  The CUDA
 runtime is linked statically and the driver's tensor-map encoder is looked up
 at run time, so the library loads on a machine without a GPU.
 """
@@ -57,8 +57,9 @@ def up_to_date(variant: str = "") -> bool:
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
-# (CTAs per unit, output type) variants of the kernel, one object file each
-VARIANTS = [(cluster, out) for cluster in (1, 2, 4) for out in (0, 1, 2)]
+# (CTAs per unit, output type, operand width) variants of the kernel, one
+# object file each
+VARIANTS = [(cluster, out, inp) for cluster in (1, 2, 4) for out in (0, 1, 2) for inp in (0, 1)]
 
 
 def _compile(args):
@@ -84,9 +85,9 @@ def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
     if verbose:
         common.insert(1, "-Xptxas=-v")
     jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose)]
-    for cluster, out in VARIANTS:
-        obj = os.path.join(objdir, f"kernels_c{cluster}_o{out}.o")
-        jobs.append((common + [f"-DGEMM_INST_CLUSTER={cluster}", f"-DGEMM_INST_OUT={out}",
+    for cluster, out, inp in VARIANTS:
+        obj = os.path.join(objdir, f"kernels_c{cluster}_o{out}_i{inp}.o")
+        jobs.append((common + [f"-DGEMM_INST_CLUSTER={cluster}", f"-DGEMM_INST_OUT={out}", f"-DGEMM_INST_IN={inp}",
                                os.path.join(CSRC, "kernels_inst.cu"), "-o", obj], verbose))
     workers = max(1, min(len(jobs), os.cpu_count() or 1))
     with ThreadPoolExecutor(workers) as ex:

@@ -36,12 +36,17 @@ std::mutex g_mu;
 std::vector<gemm_plan*> g_plans[kMaxDevices];  // live plans per device, newest last
 EncodeTiledFn g_encode = nullptr;
 
-int elem_bytes(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+bool is_fp8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
+int elem_bytes(int dt) { return dt == GEMM_F32 ? 4 : is_fp8(dt) ? 1 : 2; }
+// K elements per k-block: one 128-byte swizzle row.
+int64_t kblock_elems(int in_dtype) { return kBlockKBytes / elem_bytes(in_dtype); }
 
 CUtensorMapDataType tma_dtype(int dt) {
     switch (dt) {
         case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case GEMM_E4M3:
+        case GEMM_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes moved as they are
         default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -80,8 +85,11 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }
 
+// tcgen05 instruction descriptor: f32 accumulator, A and B K-major, M×N.
+// Operand format field (bits 7-9 for A, 10-12 for B): kind::f16 reads
+// 0 = f16, 1 = bf16; kind::f8f6f4 reads 0 = E4M3, 1 = E5M2.
 uint32_t make_idesc(int in_dtype, int m, int n) {
-    const uint32_t ab = in_dtype == GEMM_BF16 ? 1u : 0u;  // operand format: 0 = f16, 1 = bf16
+    const uint32_t ab = (in_dtype == GEMM_BF16 || in_dtype == GEMM_E5M2) ? 1u : 0u;
     return (1u << 4)                   // accumulator format: f32
            | (ab << 7) | (ab << 10)    // A and B formats
            | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);  // both K-major (bits 15/16 = 0)
@@ -124,7 +132,7 @@ namespace {
 
 // Pure host checks, no CUDA call: shared by every run entry point.
 int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype) {
-    if (dtype != GEMM_BF16 && dtype != GEMM_F16) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_BF16 && dtype != GEMM_F16 && !is_fp8(dtype)) return GEMM_ERR_INVALID_ARG;
     if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -134,7 +142,7 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0) return GEMM_ERR_MISALIGNED;
     if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0))
         return GEMM_ERR_MISALIGNED;
-    if ((K * 2) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    if ((K * elem_bytes(dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     if ((N * elem_bytes(out_dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     return GEMM_OK;
 }
@@ -145,9 +153,9 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
 // 32-byte sector, the load path becomes the bound, and halving the B reads
 // wins (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of
 // all SMs wins (4-CTA clusters fit on 144 of the 152 SMs).
-int unit_ctas(const gemm_plan* plan, int64_t K) {
+int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype) {
     if (plan->pair != 2) return 1;
-    const bool mc = plan->multicast == 1 || (plan->multicast < 0 && (K * 2) % 128 != 0);
+    const bool mc = plan->multicast == 1 || (plan->multicast < 0 && (K * elem_bytes(in_dtype)) % 128 != 0);
     return mc ? 4 : 2;
 }
 
@@ -190,9 +198,9 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
-    const int cluster = unit_ctas(plan, K);
+    const int cluster = unit_ctas(plan, K, dtype);
     const int bn = choose_tile_n(plan, M, N, cluster);
-    const KernelInfo ki = kernel_info(cluster, bn, out_dtype);
+    const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * cluster;
     Params p;
@@ -201,7 +209,8 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.K = (int)K;
     p.tiles_m = (int)((M + tile_m - 1) / tile_m);
     p.tiles_n = (int)((N + bn - 1) / bn);
-    p.k_blocks = (int)((K + kBlockK - 1) / kBlockK);
+    const int64_t kbe = kblock_elems(dtype);
+    p.k_blocks = (int)((K + kbe - 1) / kbe);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
@@ -217,10 +226,10 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.trace = plan->d_trace;
 
     CUtensorMap tmA, tmB, tmC;
-    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B,
+    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), kBlockK,
+        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), (uint32_t)kbe,
                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
@@ -283,9 +292,9 @@ size_t trace_bytes(const gemm_plan* plan) {
 int query_capacity(gemm_plan* plan, int cluster) {
     int max_smem = 0;
     KernelFn probe = nullptr;
-    for (int out = 0; out < 3; ++out) {
+    for (int v = 0; v < 6; ++v) {   // output type × operand width
         for (int i = 0; i < kNumTileWidths; ++i) {
-            const KernelInfo ki = kernel_info(cluster, kTileWidths[i], out);
+            const KernelInfo ki = kernel_info(cluster, kTileWidths[i], v % 3, v / 3);
             if (ki.fn == nullptr) continue;
             if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem_bytes) !=
                 cudaSuccess) {
@@ -443,7 +452,7 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
     int rc = validate(A_host, B_host, C_host, M, N, K, dtype, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes[3] = {(size_t)M * (size_t)K * 2, (size_t)N * (size_t)K * 2,
+    const size_t bytes[3] = {(size_t)M * (size_t)K * elem_bytes(dtype), (size_t)N * (size_t)K * elem_bytes(dtype),
                              (size_t)M * (size_t)N * (size_t)elem_bytes(out_dtype)};
     std::lock_guard<std::mutex> lk(plan->host_mu);
     for (int i = 0; i < 3; ++i) {

@@ -91,16 +91,17 @@ enum TraceSlot {
 
 constexpr int kNumThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr int kBlockK = 64;              // one 128-byte swizzle row of 16-bit elements
-constexpr int kMmaK = 16;                // K of one kind::f16 MMA (32 bytes)
+constexpr int kBlockKBytes = 128;        // K bytes per k-block: one 128-byte swizzle row
+constexpr int kMmaKBytes = 32;           // K bytes of one MMA (16 bf16/f16 or 32 fp8 elements)
 constexpr int kRowsPerCta = 128;         // TMEM lanes = rows of A per CTA
 constexpr int kAccStride = 256;          // TMEM columns between the two accumulators
 constexpr int kTmemCols = 2 * kAccStride;
-constexpr int kStageBytesA = kRowsPerCta * kBlockK * 2;
+constexpr int kStageBytesA = kRowsPerCta * kBlockKBytes;
 constexpr int kChunkCols = 32;           // accumulator columns per epilogue store box
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any single wait
 
 constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2;
+constexpr int kIn16 = 0, kInF8 = 1;      // operand width: bf16/f16 (kind::f16) or E4M3/E5M2 (kind::f8f6f4)
 constexpr int kErrCuda = -4;      // device side: the launch's shared memory is not 1 KB aligned
 constexpr int kErrTimeout = -7;
 constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the base address
@@ -125,8 +126,11 @@ constexpr int kFixupBytes = kPartialFloats * 4;   // shared memory per epilogue 
 // CTA pair issuing cta_group::2 MMAs) or 4 (two pairs stacked along M that
 // share the B tile: each CTA loads a quarter of it and multicasts it to
 // the same-rank CTA of the other pair).  kBN: tile width (accumulator
-// columns, a multiple of 32 up to 256).  kOut: C element type.
-template <int kCluster, int kBN, int kOut>
+// columns, a multiple of 32 up to 256).  kOut: C element type.  kIn:
+// operand width; a k-block is one 128-byte swizzle row of K either way
+// (64 bf16/f16 or 128 fp8 elements), so shared-memory layout, descriptors
+// and the ring are the same for both.
+template <int kCluster, int kBN, int kOut, int kIn>
 struct Cfg {
     static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "1, 2 or 4 CTAs per unit");
     static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "tile width");
@@ -136,8 +140,9 @@ struct Cfg {
     static constexpr int kRowsB = kBN / kPair;                    // B rows held per CTA
     static constexpr int kRowsBLoad = kBN / kCluster;             // B rows each CTA loads
     static_assert(kRowsBLoad % 8 == 0, "B boxes must fill 1 KB swizzle atoms");
-    static constexpr int kStageBytesB = kRowsB * kBlockK * 2;
-    static constexpr int kLoadBytesB = kRowsBLoad * kBlockK * 2;
+    static constexpr int kBlockKElems = kIn == kInF8 ? kBlockKBytes : kBlockKBytes / 2;   // TMA K coordinate step
+    static constexpr int kStageBytesB = kRowsB * kBlockKBytes;
+    static constexpr int kLoadBytesB = kRowsBLoad * kBlockKBytes;
     static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
     static constexpr int kOutBytes = kOut == kOutF32 ? 4 : 2;
     static constexpr int kRowBytes = kChunkCols * kOutBytes;    // 128 (fp32) or 64 (16-bit)
@@ -249,11 +254,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
     }
 }
 
-template <int kCluster, int kBN, int kOut>
+template <int kCluster, int kBN, int kOut, int kIn>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tn_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const Params p) {
-    using C = Cfg<kCluster, kBN, kOut>;
+    using C = Cfg<kCluster, kBN, kOut, kIn>;
     constexpr int kPair = C::kPair;
     constexpr int kStages = C::kStages;
     constexpr int kChunks = kBN / kChunkCols;
@@ -375,16 +380,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             // this CTA and to the same-rank CTA of the other pair
                             const uint32_t fb_leader = map_shared_rank(fb, leader);
                             const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
+                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * C::kBlockKElems, a_row);
                             tma_load_2d_pair_multicast(b_dst + pidx * C::kLoadBytesB, &tmB, fb_leader, mask,
-                                                       kb * kBlockK, b_row);
+                                                       kb * C::kBlockKElems, b_row);
                         } else if constexpr (kCluster == 2) {
                             const uint32_t fb_leader = map_shared_rank(fb, leader);
-                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * kBlockK, a_row);
-                            tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * kBlockK, b_row);
+                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * C::kBlockKElems, a_row);
+                            tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * C::kBlockKElems, b_row);
                         } else {
-                            tma_load_2d(a_dst, &tmA, fb, kb * kBlockK, a_row);
-                            tma_load_2d(b_dst, &tmB, fb, kb * kBlockK, b_row);
+                            tma_load_2d(a_dst, &tmA, fb, kb * C::kBlockKElems, a_row);
+                            tma_load_2d(b_dst, &tmB, fb, kb * C::kBlockKElems, b_row);
                         }
                     }
                     __syncwarp();
@@ -439,9 +444,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (issuer) {
                         tc_fence_after_sync();
 #pragma unroll
-                        for (int j = 0; j < kBlockK / kMmaK; ++j) {
+                        for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
                             // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
-                            tc_mma_f16<kPair>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
+                            tc_mma<kPair, kIn == kInF8>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
                         }
                         // release the slot in every CTA whose copies write into this pair's slot
                         if constexpr (kCluster == 4) tc_commit_pair(empty_bar(stage), 0xF);

@@ -1,7 +1,7 @@
 // kernel_table.h -- the instantiated variants of the persistent GEMM kernel.
 //
-// kernels_inst.cu is compiled once per (CTAs per unit, output type); each
-// object defines one lookup function over the tile widths.  The host side
+// kernels_inst.cu is compiled once per (CTAs per unit, output type, operand
+// width); each object defines one lookup function over the tile widths.  The host side
 // (gemm_api.cu) picks a variant through gb300::kernel_info().
 #pragma once
 #include <cuda.h>
@@ -20,24 +20,40 @@ struct KernelInfo {
 constexpr int kNumTileWidths = 5;
 constexpr int kTileWidths[kNumTileWidths] = {256, 224, 192, 160, 128};
 
-KernelInfo kernel_info_c1_o0(int bn);
-KernelInfo kernel_info_c1_o1(int bn);
-KernelInfo kernel_info_c1_o2(int bn);
-KernelInfo kernel_info_c2_o0(int bn);
-KernelInfo kernel_info_c2_o1(int bn);
-KernelInfo kernel_info_c2_o2(int bn);
-KernelInfo kernel_info_c4_o0(int bn);
-KernelInfo kernel_info_c4_o1(int bn);
-KernelInfo kernel_info_c4_o2(int bn);
+KernelInfo kernel_info_c1_o0_i0(int bn);
+KernelInfo kernel_info_c1_o0_i1(int bn);
+KernelInfo kernel_info_c1_o1_i0(int bn);
+KernelInfo kernel_info_c1_o1_i1(int bn);
+KernelInfo kernel_info_c1_o2_i0(int bn);
+KernelInfo kernel_info_c1_o2_i1(int bn);
+KernelInfo kernel_info_c2_o0_i0(int bn);
+KernelInfo kernel_info_c2_o0_i1(int bn);
+KernelInfo kernel_info_c2_o1_i0(int bn);
+KernelInfo kernel_info_c2_o1_i1(int bn);
+KernelInfo kernel_info_c2_o2_i0(int bn);
+KernelInfo kernel_info_c2_o2_i1(int bn);
+KernelInfo kernel_info_c4_o0_i0(int bn);
+KernelInfo kernel_info_c4_o0_i1(int bn);
+KernelInfo kernel_info_c4_o1_i0(int bn);
+KernelInfo kernel_info_c4_o1_i1(int bn);
+KernelInfo kernel_info_c4_o2_i0(int bn);
+KernelInfo kernel_info_c4_o2_i1(int bn);
 
-// cluster: CTAs per work unit (1, 2 or 4); out: 0 bf16, 1 f16, 2 fp32.
-inline KernelInfo kernel_info(int cluster, int bn, int out) {
+// cluster: CTAs per work unit (1, 2 or 4); out: 0 bf16, 1 f16, 2 fp32;
+// in: 0 bf16/f16 operands, 1 E4M3/E5M2 operands.
+inline KernelInfo kernel_info(int cluster, int bn, int out, int in) {
+#define GB300_PICK(C)                                                                                  \
+    (in == 0 ? (out == 0 ? kernel_info_c##C##_o0_i0(bn) : out == 1 ? kernel_info_c##C##_o1_i0(bn)     \
+                                                                   : kernel_info_c##C##_o2_i0(bn))    \
+             : (out == 0 ? kernel_info_c##C##_o0_i1(bn) : out == 1 ? kernel_info_c##C##_o1_i1(bn)     \
+                                                                   : kernel_info_c##C##_o2_i1(bn)))
     switch (cluster) {
-        case 1: return out == 0 ? kernel_info_c1_o0(bn) : out == 1 ? kernel_info_c1_o1(bn) : kernel_info_c1_o2(bn);
-        case 2: return out == 0 ? kernel_info_c2_o0(bn) : out == 1 ? kernel_info_c2_o1(bn) : kernel_info_c2_o2(bn);
-        case 4: return out == 0 ? kernel_info_c4_o0(bn) : out == 1 ? kernel_info_c4_o1(bn) : kernel_info_c4_o2(bn);
+        case 1: return GB300_PICK(1);
+        case 2: return GB300_PICK(2);
+        case 4: return GB300_PICK(4);
         default: return KernelInfo{nullptr, 0, 0};
     }
+#undef GB300_PICK
 }
 
 }  // namespace gb300

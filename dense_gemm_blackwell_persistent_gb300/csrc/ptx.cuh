@@ -243,24 +243,25 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] · B[smem desc]ᵀ, kind::f16 (bf16/f16 in, fp32 acc).
-template <int kCtaGroup>
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    if constexpr (kCtaGroup == 2)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-            : "memory");
+// D[tmem] (+)= A[smem desc] · B[smem desc]ᵀ with an fp32 accumulator.
+// kF8 selects the instruction kind: kind::f16 (bf16/f16 operands, K = 16
+// elements = 32 bytes per instruction) or kind::f8f6f4 (E4M3/E5M2
+// operands, K = 32 elements, again 32 bytes).  The operand formats
+// themselves are fields of the instruction descriptor.
+template <int kCtaGroup, bool kF8>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+#define GB300_TC_MMA(GROUP, KIND)                                                                       \
+    asm volatile("{\n\t.reg .pred p;\n\t"                                                               \
+                 "setp.ne.b32 p, %4, 0;\n\t"                                                           \
+                 "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem), \
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)                                  \
+                 : "memory")
+    if constexpr (kCtaGroup == 2 && kF8) GB300_TC_MMA("2", "f8f6f4");
+    else if constexpr (kCtaGroup == 2) GB300_TC_MMA("2", "f16");
+    else if constexpr (kF8) GB300_TC_MMA("1", "f8f6f4");
+    else GB300_TC_MMA("1", "f16");
+#undef GB300_TC_MMA
 }
 
 // Arrive once on `bar` when every tcgen05 op this thread issued so far has

@@ -2,9 +2,9 @@
  * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
  *
  * Operation.  C = A·Bᵀ: A is M×K row-major, B is stored transposed as N×K
- * row-major, C is M×N row-major.  Inputs are bf16 or f16 (both the same
- * type), products are accumulated in fp32, and C is written as fp32, bf16 or
- * f16 (rounded to nearest, ties to even).  This is the problem statement of
+ * row-major, C is M×N row-major.  Inputs are bf16, f16, E4M3 or E5M2
+ * (both the same type), products are accumulated in fp32, and C is written
+ * as fp32, bf16 or f16 (rounded to nearest, ties to even).  This is the problem statement of
  * "Optimizing Blackwell Matrix Multiplication in Mojo (Part 2)" (intro and
  * "Kernel 2: TMA and Tensor Core": B kept N×K so that both operands are read
  * along K), with the bf16-in / fp32-accumulate / cast-once-at-the-end
@@ -18,8 +18,9 @@
  *
  * Layout rules (checked on the host before anything is launched):
  *   - A, B, C 16-byte aligned;
- *   - K * 2 bytes and N * sizeof(C element) bytes multiples of 16, i.e.
- *     K % 8 == 0 and N % 8 == 0 (bf16/f16 out) or N % 4 == 0 (fp32 out);
+ *   - K * sizeof(input element) and N * sizeof(C element) bytes multiples
+ *     of 16, i.e. K % 8 == 0 (bf16/f16 in) or K % 16 == 0 (fp8 in), and
+ *     N % 8 == 0 (bf16/f16 out) or N % 4 == 0 (fp32 out);
  *   - M, N, K < 2^31.
  * Other shapes return GEMM_ERR_UNSUPPORTED: there is no slow fallback path.
  *
@@ -36,7 +37,9 @@
  *
  * Threads.  A plan may be used from several host threads and streams at
  * once; calls build their tensor maps on the host stack and share only
- * read-only plan state plus the device status word.
+ * read-only plan state plus the device status word.  Exception: with the
+ * stream-K option on (off by default) runs share the plan's workspace, so
+ * runs that may overlap on the GPU must then use different plans.
  */
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H
@@ -48,7 +51,15 @@
 extern "C" {
 #endif
 
-typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+/* Element types.  Inputs (A and B, both the same type): BF16, F16, E4M3,
+ * E5M2.  Output C: F32, BF16, F16.  E4M3 is the finite-only 8-bit format
+ * (4 exponent bits, bias 7, 3 fraction bits, no infinities, S.1111.111 the
+ * only NaN) and E5M2 the IEEE-style one (5 exponent bits, bias 15, 2
+ * fraction bits): the float8_e4m3fn and float8_e5m2 operand types of
+ * "Writing Mosaic GPU kernels with Pallas", "Blackwell (tcgen05)", "Issuing
+ * the operation".  8-bit inputs are multiplied exactly and summed in fp32
+ * like the 16-bit ones, at twice the tensor-core rate; no scale factors. */
+typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4 } gemm_dtype_t;
 
 typedef enum {
     GEMM_OK = 0,
@@ -99,7 +110,8 @@ int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
 int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value);
 
 /* C = A·Bᵀ on `stream` with the most recently created plan of the current
- * device that is still alive (GEMM_ERR_NO_PLAN if none).  dtype: GEMM_BF16 or GEMM_F16 (A and B);
+ * device that is still alive (GEMM_ERR_NO_PLAN if none).  dtype: GEMM_BF16, GEMM_F16, GEMM_E4M3 or
+ * GEMM_E5M2 (A and B);
  * out_dtype: GEMM_F32, GEMM_BF16 or GEMM_F16.  Asynchronous. */
 int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
              int dtype, int out_dtype, void* stream);

@@ -55,6 +55,8 @@ def test_host_validation_without_gpu(lib):
     # bad dtype pair
     assert rs("gemm_run", good, good, good, 64, 64, 64, 2, 2, None) == lib.GEMM_ERR_INVALID_ARG
     assert rs("gemm_run", good, good, good, 64, 64, 64, 0, 7, None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_run", good, good, good, 64, 64, 64, 5, 2, None) == lib.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_run", good, good, good, 64, 64, 64, 0, 3, None) == lib.GEMM_ERR_INVALID_ARG   # fp8 out
     # negative sizes
     assert rs("gemm_run", good, good, good, -1, 64, 64, 0, 2, None) == lib.GEMM_ERR_INVALID_ARG
     # null pointers
@@ -63,8 +65,10 @@ def test_host_validation_without_gpu(lib):
     # misaligned pointers
     assert rs("gemm_run", vp((1 << 20) + 8), good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_MISALIGNED
     assert rs("gemm_run", good, good, vp((1 << 20) + 4), 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_MISALIGNED
-    # pitches TMA cannot address
+    # pitches TMA cannot address (K bytes and N bytes multiples of 16)
     assert rs("gemm_run", good, good, good, 64, 64, 60, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_run", good, good, good, 64, 64, 24, 3, 2, None) == lib.GEMM_ERR_UNSUPPORTED   # fp8: K % 16
+    assert rs("gemm_run", good, good, good, 64, 64, 24, 4, 2, None) == lib.GEMM_ERR_UNSUPPORTED
     assert rs("gemm_run", good, good, good, 64, 6, 64, 0, 0, None) == lib.GEMM_ERR_UNSUPPORTED
     assert rs("gemm_run", good, good, good, 64, 2, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
     assert rs("gemm_run", good, good, good, 1 << 31, 64, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED

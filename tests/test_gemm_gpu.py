@@ -16,7 +16,9 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 OUTS = [wl.F32, wl.BF16, wl.F16]
+FP8S = [wl.E4M3, wl.E5M2]
 TORCH = wl.TORCH_DTYPES
+CODE_OF = {t: code for code, t in wl.TORCH_DTYPES.items()}
 
 
 @pytest.fixture(scope="module")
@@ -59,7 +61,7 @@ def run(g, plan, A, B, out_dtype, C=None):
     N = B.shape[0]
     if C is None:
         C = torch.full((M, N), float("nan"), dtype=TORCH[out_dtype], device="cuda")
-    code = wl.BF16 if A.dtype == torch.bfloat16 else wl.F16
+    code = CODE_OF[A.dtype]
     g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, code, out_dtype,
                     torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
@@ -68,8 +70,7 @@ def run(g, plan, A, B, out_dtype, C=None):
 
 
 def oracle_full(A, B):
-    dt = wl.BF16 if A.dtype == torch.bfloat16 else wl.F16
-    return oracle.gemm(wl.as_bits(A), wl.as_bits(B), dt)
+    return oracle.gemm(wl.as_bits(A), wl.as_bits(B), CODE_OF[A.dtype])
 
 
 def draw(M, N, K, dtype=wl.BF16, dist="normal", seed=0):
@@ -252,9 +253,70 @@ def test_stream_k_off_matches_within_tolerance(g, fresh_plan):
     parity.assert_within(C_off, C_ref, S, wl.F32, "stream-K off")
 
 
+# ------------------------------------------------------------------ 8-bit float inputs
+
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("fp8", FP8S, ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("out", OUTS)
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 272), (384, 512, 1024), (1100, 520, 144)])
+def test_fp8_integer_inputs_bit_exact(g, plan, unit, fp8, out, shape):
+    """Integers -4..4 are exact in both 8-bit formats and every partial sum is
+    exact in fp32: any correct kernel gives the oracle's bits.  K = 272 and
+    144 end in a partial 128-element k-block (zero-filled by TMA)."""
+    M, N, K = shape
+    configure(g, plan, unit)
+    try:
+        w = wl.Workload("case", M, N, K, fp8, out, "int", 40 + K, lo=-4, hi=4)
+        A, B = wl.make_inputs(w)
+        C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), out))
+        C_ref, _ = oracle_full(A, B)
+        want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(C, want), f"{int((C != want).sum())} mismatches"
+    finally:
+        configure(g, plan, 4)
+
+
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("fp8", FP8S, ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("shape", [(512, 384, 2048), (1000, 760, 1264)])
+def test_fp8_random_within_tolerance(g, plan, unit, fp8, shape):
+    M, N, K = shape
+    configure(g, plan, unit)
+    try:
+        w = wl.Workload("case", M, N, K, fp8, wl.F32, "normal", 50 + K)
+        A, B = wl.make_inputs(w)
+        Ad, Bd = A.cuda(), B.cuda()
+        C_ref, S = oracle_full(A, B)
+        for out in OUTS:
+            C = parity.to_f64(run(g, plan, Ad, Bd, out))
+            parity.assert_within(C, C_ref, S, out, f"fp8 {fp8} {shape} unit={unit} out={out}")
+    finally:
+        configure(g, plan, 4)
+
+
+def test_fp8_matmul_helper(g, plan):
+    w = wl.Workload("case", 300, 264, 400, wl.E4M3, wl.BF16, "int", 61, lo=-4, hi=4)
+    A, B = wl.make_inputs(w)
+    C = g.matmul(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert C.dtype == torch.bfloat16
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(parity.to_f64(C), oracle.decode(oracle.encode(C_ref, wl.BF16), wl.BF16))
+
+
+def test_fp8_k_must_fill_16_bytes(g, plan):
+    A = torch.zeros((64, 24), dtype=torch.float8_e4m3fn, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    import ctypes
+    vp = ctypes.c_void_p
+    assert g.raw_status("gemm_plan_run", vp(plan), vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()),
+                        64, 64, 24, g.GEMM_E4M3, g.GEMM_F32, None) == g.GEMM_ERR_UNSUPPORTED
+
+
 # ------------------------------------------------------------------ full-size workloads
 
-FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16"]
+FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16",
+        "gemm_4096_e4m3"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -13,13 +13,18 @@ Workloads follow the shapes the pages measure on:
   * a ragged shape that is a multiple of no tile, the case the masked matmul
     of "Chapter 7: Writing Custom Kernels with Pallas", §4.3 exists for.
   * a small 256³ case and an 8192³ case.
+  * bf16 4096³'s shape with 8-bit float inputs (E4M3, bf16 out): the
+    float8_e4m3fn operand type of "Writing Mosaic GPU kernels with Pallas",
+    "Blackwell (tcgen05)", "Issuing the operation".
 
 Recipe (one reading, stated once): a CPU ``torch.Generator`` seeded with the
 workload's seed draws A first, then B, in float32 (``randn`` for normal,
 ``rand`` scaled to [lo, hi) for uniform, ``randint`` for integers), and torch
 casts to bf16/f16 with round-to-nearest-even.  "N(0, 1/sqrt(K))" is read as
 standard deviation 1/sqrt(K).  "integers uniform in [-4, 4]" is read as the
-nine integers -4..4 inclusive.
+nine integers -4..4 inclusive.  8-bit float inputs are drawn the same way
+and cast by torch to float8_e4m3fn / float8_e5m2 (nearest, ties to even;
+N(0,1) stays far inside both ranges).
 """
 from __future__ import annotations
 
@@ -30,10 +35,12 @@ from typing import Optional
 import numpy as np
 import torch
 
-BF16, F16, F32 = 0, 1, 2           # dtype codes shared with the C ABI's gemm_dtype_t
-DTYPE_NAMES = {BF16: "bf16", F16: "f16", F32: "f32"}
-TORCH_DTYPES = {BF16: torch.bfloat16, F16: torch.float16, F32: torch.float32}
-ELEM_BYTES = {BF16: 2, F16: 2, F32: 4}
+BF16, F16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4   # dtype codes shared with the C ABI's gemm_dtype_t
+FP8 = (E4M3, E5M2)
+DTYPE_NAMES = {BF16: "bf16", F16: "f16", F32: "f32", E4M3: "e4m3", E5M2: "e5m2"}
+TORCH_DTYPES = {BF16: torch.bfloat16, F16: torch.float16, F32: torch.float32,
+                E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+ELEM_BYTES = {BF16: 2, F16: 2, F32: 4, E4M3: 1, E5M2: 1}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -76,6 +83,7 @@ WORKLOADS = {
                                            "uniform", 3, lo=-1.0, hi=1.0),
     "gemm_8192_bf16": Workload("gemm_8192_bf16", 8192, 8192, 8192, BF16, BF16, "normal", 4,
                                std=1.0 / math.sqrt(8192)),
+    "gemm_4096_e4m3": Workload("gemm_4096_e4m3", 4096, 4096, 4096, E4M3, BF16, "normal", 5),
 }
 
 
@@ -112,7 +120,9 @@ def make_inputs(w: Workload, M: Optional[int] = None, N: Optional[int] = None,
 
 
 def as_bits(t: torch.Tensor) -> np.ndarray:
-    """The raw 16-bit patterns of a bf16/f16 CPU tensor, as a uint16 numpy array."""
+    """The raw bit patterns of a CPU input tensor: uint16 for bf16/f16, uint8 for fp8."""
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.contiguous().view(torch.uint8).numpy()
     assert t.dtype in (torch.bfloat16, torch.float16)
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
