@@ -29,6 +29,8 @@ GEMM_ERR_TIMEOUT = -7
 GEMM_ERR_NO_DEVICE = -8
 GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N, GEMM_OPT_STREAM_K = 1, 2, 3, 4, 5
 GEMM_OPT_MULTICAST = 6
+GEMM_OPT_WAIT_LIMIT_US = 7
+GEMM_OPT_STALL_TEST = 8
 
 # GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps).
 VARIANT = os.environ.get("GB300_GEMM_VARIANT", "")

@@ -114,6 +114,8 @@ struct gemm_plan {
     int cap_ctas = 0;
     int tile_n = 0;               // 0 = 256
     int stream_k = 0;             // split the K work of a partial last wave (option)
+    int64_t wait_limit_us = 0;    // bound on a kernel wait (0 = kWaitLimitNs)
+    int stall_test = 0;           // tests of the timeout path only
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
@@ -223,6 +225,8 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
     p.partials = plan->d_partials;
     p.flags = plan->d_flags;
+    p.wait_limit_ns = plan->wait_limit_us > 0 ? (unsigned long long)plan->wait_limit_us * 1000ull : kWaitLimitNs;
+    p.stall_test = plan->stall_test;
     p.trace = plan->d_trace;
 
     CUtensorMap tmA, tmB, tmC;
@@ -403,6 +407,14 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
         case GEMM_OPT_STREAM_K:
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             plan->stream_k = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_WAIT_LIMIT_US:
+            if (value < 0 || value > 60000000) return GEMM_ERR_INVALID_ARG;
+            plan->wait_limit_us = value;
+            return GEMM_OK;
+        case GEMM_OPT_STALL_TEST:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            plan->stall_test = (int)value;
             return GEMM_OK;
         case GEMM_OPT_TILE_N: {
             if (value == 0) {

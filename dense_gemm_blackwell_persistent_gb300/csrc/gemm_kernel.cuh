@@ -98,7 +98,8 @@ constexpr int kAccStride = 256;          // TMEM columns between the two accumul
 constexpr int kTmemCols = 2 * kAccStride;
 constexpr int kStageBytesA = kRowsPerCta * kBlockKBytes;
 constexpr int kChunkCols = 32;           // accumulator columns per epilogue store box
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on any single wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default bound on any single wait
+constexpr int kRoleStallTest = 8;  // status[1] of the timeout a test provokes on purpose
 
 constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2;
 constexpr int kIn16 = 0, kInF8 = 1;      // operand width: bf16/f16 (kind::f16) or E4M3/E5M2 (kind::f8f6f4)
@@ -114,6 +115,8 @@ struct Params {
     Schedule sched;    // whole-tile waves + stream-K part
     float* partials;   // stream-K: one partial-tile slot per unit, or null
     int* flags;        // stream-K: "partial published" per (split tile, CTA, epilogue warp)
+    unsigned long long wait_limit_ns;   // bound on any single wait
+    int stall_test;    // 1: the MMA warp waits on a barrier nothing completes (tests of the timeout path)
     unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
 };
 
@@ -199,7 +202,7 @@ __device__ __forceinline__ void record_error(const Params& p, int role, int deta
     }
 }
 
-// Wait for the phase of parity `parity` of `bar`, for at most kWaitLimitNs.
+// Wait for the phase of parity `parity` of `bar`, for at most p.wait_limit_ns.
 // Returns false (and raises the CTA's abort flag) if the bound expires or
 // another role of this CTA has already aborted.
 template <bool kClusterScope>
@@ -210,7 +213,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     while (true) {
         if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > p.wait_limit_ns) {
             record_error(p, role, detail);
             *abort_flag = 1;
             return false;
@@ -218,7 +221,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
-// Wait until *flag == 1 (another CTA's release), for at most kWaitLimitNs:
+// Wait until *flag == 1 (another CTA's release), for at most p.wait_limit_ns:
 // lane 0 polls, the warp gets the outcome.  On expiry records a timeout and
 // raises the CTA's abort flag; gives up early if another role aborted.
 __device__ __forceinline__ bool wait_flag_bounded(const int* flag, volatile uint32_t* abort_flag, const Params& p,
@@ -233,7 +236,7 @@ __device__ __forceinline__ bool wait_flag_bounded(const int* flag, volatile uint
                 ok = 0;
                 break;
             }
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > p.wait_limit_ns) {
                 record_error(p, role, detail);
                 *abort_flag = 1;
                 ok = 0;
@@ -416,6 +419,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             int i = 0;
             uint64_t full_wait_ns = 0, acc_wait_ns = 0;   // trace builds only
             const int nwork = work_count(p.sched, pair_id);
+            if (p.stall_test) {
+                // A wait that cannot end: fix_bar(0) gets no arrival unless a
+                // stream-K finisher uses it, and this launch has none.  It runs
+                // out after p.wait_limit_ns and takes the kernel down the
+                // timeout path (status, abort flag, orderly teardown).
+                ok = __all_sync(0xffffffffu, wait_bounded<false>(fix_bar(0), 0, abort_flag, p, kRoleStallTest, 0));
+            }
             for (; i < nwork && ok; ++i) {
                 const Work w = work_item(p.sched, pair_id, i);
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;

@@ -89,11 +89,18 @@ typedef enum {
     GEMM_OPT_STREAM_K = 5,       /* 1: spread the K work of a partial last wave over all
                                     resident units (stream-K tail, deterministic
                                     fixup); 0 (default): whole tiles only              */
-    GEMM_OPT_MULTICAST = 6       /* with CTA pairs: 1 = two pairs per 4-CTA cluster work
+    GEMM_OPT_MULTICAST = 6,      /* with CTA pairs: 1 = two pairs per 4-CTA cluster work
                                     on vertically adjacent tiles and share their B tile
                                     through TMA multicast (512×BN per cluster); 0 = one
                                     pair per cluster; -1 (default) = multicast when the
                                     rows of A and B are not a multiple of 128 bytes   */
+    GEMM_OPT_WAIT_LIMIT_US = 7,  /* bound on any single wait inside the kernel, in µs,
+                                    1..60e6 (0 = default: 2 s)                         */
+    GEMM_OPT_STALL_TEST = 8      /* tests of the timeout path only: 1 = the MMA warp
+                                    first waits on a barrier nothing completes, so the
+                                    run ends, after about two wait bounds, with
+                                    GEMM_ERR_TIMEOUT (role 8) in the status word and
+                                    C unwritten; 0 (default) = off                     */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan

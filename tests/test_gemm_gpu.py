@@ -398,6 +398,46 @@ def test_error_codes(g, plan):
     assert g.gemm_plan_status(plan) == 0
 
 
+@pytest.mark.parametrize("unit", UNITS)
+def test_bounded_wait_expires_and_plan_recovers(g, fresh_plan, unit):
+    """Failure detection without a GPU fault: with the test option on, the MMA
+    warp waits on a barrier nothing completes.  The wait runs out after the
+    shortened bound, the kernel records GEMM_ERR_TIMEOUT, the other roles
+    leave their loops (abort flag, or their own bound in the peer CTAs), the
+    CTAs tear down in order, and the same plan then computes correctly."""
+    import time
+    configure(g, fresh_plan, unit)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_WAIT_LIMIT_US, 20000)   # 20 ms
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STALL_TEST, 1)
+    A, B = draw(512, 520, 512, dist="int", seed=9)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = torch.full((512, 520), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), 512, 520, 512, wl.BF16, wl.F32,
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert g.gemm_plan_status(fresh_plan) == g.GEMM_ERR_TIMEOUT
+    assert elapsed < 2.0, f"the timeout path took {elapsed:.2f} s for a 20 ms bound"
+    assert g.gemm_plan_status(fresh_plan) == g.GEMM_OK, "status is cleared once read"
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STALL_TEST, 0)
+    C = parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32))
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(C, C_ref)
+
+
+def test_wait_options_are_checked(g, fresh_plan):
+    import ctypes
+    p = ctypes.c_void_p(fresh_plan)
+    assert g.raw_status("gemm_plan_set_option", p, g.GEMM_OPT_WAIT_LIMIT_US, ctypes.c_int64(-1)) \
+        == g.GEMM_ERR_INVALID_ARG
+    assert g.raw_status("gemm_plan_set_option", p, g.GEMM_OPT_WAIT_LIMIT_US, ctypes.c_int64(60000001)) \
+        == g.GEMM_ERR_INVALID_ARG
+    assert g.raw_status("gemm_plan_set_option", p, g.GEMM_OPT_STALL_TEST, ctypes.c_int64(2)) \
+        == g.GEMM_ERR_INVALID_ARG
+
+
 def test_implicit_plan_and_host_entry_agree(g, plan):
     M, N, K = 520, 776, 392
     A, B = draw(M, N, K, dtype=wl.F16, seed=9)
