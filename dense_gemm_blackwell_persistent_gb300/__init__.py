@@ -31,6 +31,7 @@ GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N, GEMM_OP
 GEMM_OPT_MULTICAST = 6
 GEMM_OPT_WAIT_LIMIT_US = 7
 GEMM_OPT_STALL_TEST = 8
+GEMM_K_MAJOR, GEMM_A_MN_MAJOR, GEMM_B_MN_MAJOR = 0, 1, 2
 
 # GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps).
 VARIANT = os.environ.get("GB300_GEMM_VARIANT", "")
@@ -52,6 +53,7 @@ _lib.gemm_plan_set_option.argtypes = [_vp, _int, _i64]
 _lib.gemm_run.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
+_lib.gemm_plan_run_layout.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
 _lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
@@ -62,7 +64,7 @@ _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int)
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
-              "gemm_plan_run_host", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
+              "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
               "gemm_plan_last_launch",
               "gemm_plan_trace", "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
@@ -111,6 +113,12 @@ def gemm_plan_run(plan: int, A: int, B: int, C: int, M: int, N: int, K: int, dty
                   out_dtype: int, stream: int = 0) -> None:
     _check(_lib.gemm_plan_run(_vp(plan), _vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype,
                               _vp(stream)), "gemm_plan_run")
+
+
+def gemm_plan_run_layout(plan: int, A: int, B: int, C: int, M: int, N: int, K: int, dtype: int,
+                         out_dtype: int, layout: int, stream: int = 0) -> None:
+    _check(_lib.gemm_plan_run_layout(_vp(plan), _vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, layout,
+                                     _vp(stream)), "gemm_plan_run_layout")
 
 
 def gemm_plan_run_host(plan: int, A_host: int, B_host: int, C_host: int, M: int, N: int, K: int,
@@ -176,20 +184,31 @@ def _dtype_code(t) -> int:
     return codes[t]
 
 
-def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None):
+def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: bool = False,
+           b_kn: bool = False):
     """C = A @ B.T for CUDA tensors A [M,K], B [N,K] (contiguous; bf16, f16,
     float8_e4m3fn or float8_e5m2, both the same).
 
+    a_km / b_kn: A is given as [K,M] / B as [K,N] (both contiguous), read in
+    place by the tensor cores (16-bit inputs; needs a plan), so
+    ``matmul(A, B, b_kn=True)`` is the plain A @ B.
     out_dtype: torch.float32, torch.bfloat16 or torch.float16 (default: A's
     dtype for 16-bit inputs, bf16 for fp8 inputs).
     Runs on torch's current stream of A's device.
     """
     import torch
-    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
-        raise ValueError("A must be [M,K] and B [N,K]")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be matrices")
+    layout = (GEMM_A_MN_MAJOR if a_km else 0) | (GEMM_B_MN_MAJOR if b_kn else 0)
+    if a_km:
+        A = A.t()          # view only: the data stay K-by-M
+    if b_kn:
+        B = B.t()
+    if A.shape[1] != B.shape[1]:
+        raise ValueError("the operands' K extents differ")
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
-    if not (A.is_contiguous() and B.is_contiguous()):
+    if not ((A.t() if a_km else A).is_contiguous() and (B.t() if b_kn else B).is_contiguous()):
         raise ValueError("A and B must be contiguous row-major")
     if out_dtype is None:
         out_dtype = A.dtype if A.element_size() == 2 else torch.bfloat16
@@ -202,7 +221,11 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None):
     stream = torch.cuda.current_stream(A.device).cuda_stream
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, _dtype_code(A.dtype),
             _dtype_code(out_dtype), stream)
-    if plan is None:
+    if layout:
+        if plan is None:
+            raise ValueError("a_km / b_kn need an explicit plan (gemm_plan_run_layout)")
+        gemm_plan_run_layout(plan, *args[:-1], layout, args[-1])
+    elif plan is None:
         gemm_run(*args)
     else:
         gemm_plan_run(plan, *args)

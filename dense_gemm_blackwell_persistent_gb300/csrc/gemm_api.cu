@@ -88,11 +88,13 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t
 // tcgen05 instruction descriptor: f32 accumulator, A and B K-major, M×N.
 // Operand format field (bits 7-9 for A, 10-12 for B): kind::f16 reads
 // 0 = f16, 1 = bf16; kind::f8f6f4 reads 0 = E4M3, 1 = E5M2.
-uint32_t make_idesc(int in_dtype, int m, int n) {
+uint32_t make_idesc(int in_dtype, int m, int n, int layout) {
     const uint32_t ab = (in_dtype == GEMM_BF16 || in_dtype == GEMM_E5M2) ? 1u : 0u;
+    const uint32_t a_mn = (layout & GEMM_A_MN_MAJOR) ? 1u : 0u, b_mn = (layout & GEMM_B_MN_MAJOR) ? 1u : 0u;
     return (1u << 4)                   // accumulator format: f32
            | (ab << 7) | (ab << 10)    // A and B formats
-           | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);  // both K-major (bits 15/16 = 0)
+           | (a_mn << 15) | (b_mn << 16)   // operand majors: 0 = K-major, 1 = MN-major
+           | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // C = 0 for K == 0 (the empty sum).  `n16` 16-byte words.
@@ -133,8 +135,10 @@ struct gemm_plan {
 namespace {
 
 // Pure host checks, no CUDA call: shared by every run entry point.
-int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype) {
+int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,
+             int layout = 0) {
     if (dtype != GEMM_BF16 && dtype != GEMM_F16 && !is_fp8(dtype)) return GEMM_ERR_INVALID_ARG;
+    if (layout < 0 || layout > (GEMM_A_MN_MAJOR | GEMM_B_MN_MAJOR)) return GEMM_ERR_INVALID_ARG;
     if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -144,7 +148,11 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0) return GEMM_ERR_MISALIGNED;
     if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0))
         return GEMM_ERR_MISALIGNED;
-    if ((K * elem_bytes(dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    if (layout != 0 && is_fp8(dtype)) return GEMM_ERR_UNSUPPORTED;   // MN-major: 16-bit inputs only
+    // each operand's rows (K-major: K elements; MN-major: M or N) in 16-byte multiples
+    const int64_t ib = elem_bytes(dtype);
+    if (((layout & GEMM_A_MN_MAJOR) ? M * ib : K * ib) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+    if (((layout & GEMM_B_MN_MAJOR) ? N * ib : K * ib) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     if ((N * elem_bytes(out_dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     return GEMM_OK;
 }
@@ -155,9 +163,10 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
 // 32-byte sector, the load path becomes the bound, and halving the B reads
 // wins (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of
 // all SMs wins (4-CTA clusters fit on 144 of the 152 SMs).
-int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype) {
+int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype, int layout) {
     if (plan->pair != 2) return 1;
-    const bool mc = plan->multicast == 1 || (plan->multicast < 0 && (K * elem_bytes(in_dtype)) % 128 != 0);
+    const bool mc = plan->multicast == 1 ||
+                    (plan->multicast < 0 && layout == 0 && (K * elem_bytes(in_dtype)) % 128 != 0);
     return mc ? 4 : 2;
 }
 
@@ -173,14 +182,24 @@ int resident_units(const gemm_plan* plan, int cluster) {
 // BN + 48 (316 / 242 / 183 ns for BN = 256 / 192 / 128 with CTA pairs at
 // 8192³), so a narrower tile pays off when it fills the last wave: 224 at
 // 4096³ (4 full waves instead of 3.4) and at 1024×4096×4096.
-int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster) {
-    if (plan->tile_n > 0) return plan->tile_n;
+// A tile width an MN-major B can use: every CTA's share of the tile's B
+// rows, as held for the MMA and as loaded, whole 64-element TMA boxes.
+bool width_fits_layout(int bn, int cluster, int layout) {
+    if (!(layout & GEMM_B_MN_MAJOR)) return true;
+    const int pair = cluster >= 2 ? 2 : 1;
+    return (bn / pair) % kMnBoxElems == 0 && (bn / cluster) % kMnBoxElems == 0;
+}
+
+// Returns 0 when no width fits (a forced width the layout cannot use).
+int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int layout) {
+    if (plan->tile_n > 0) return width_fits_layout(plan->tile_n, cluster, layout) ? plan->tile_n : 0;
     const int64_t units = resident_units(plan, cluster);
     const int64_t tiles_m = (M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster);
-    int best = kTileWidths[0];
+    int best = 0;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < kNumTileWidths; ++i) {
         const int bn = kTileWidths[i];
+        if (!width_fits_layout(bn, cluster, layout)) continue;
         const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
         const int64_t cost = ((tiles + units - 1) / units) * (bn + 48);
         if (cost < best_cost) {   // ties keep the wider tile
@@ -192,7 +211,7 @@ int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster) {
 }
 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
-           int out_dtype, cudaStream_t stream) {
+           int out_dtype, cudaStream_t stream, int layout = 0) {
     if (K == 0) {
         const size_t n16 = (size_t)M * (size_t)N * elem_bytes(out_dtype) / 16;
         const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)plan->sm_count * 8);
@@ -200,8 +219,9 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
-    const int cluster = unit_ctas(plan, K, dtype);
-    const int bn = choose_tile_n(plan, M, N, cluster);
+    const int cluster = unit_ctas(plan, K, dtype, layout);
+    const int bn = choose_tile_n(plan, M, N, cluster, layout);
+    if (bn == 0) return GEMM_ERR_UNSUPPORTED;
     const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * cluster;
@@ -216,7 +236,9 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
-    p.idesc = make_idesc(dtype, kRowsPerCta * pair, bn);   // one MMA covers a pair's 256 rows
+    p.idesc = make_idesc(dtype, kRowsPerCta * pair, bn, layout);   // one MMA covers a pair's 256 rows
+    p.a_mn = (layout & GEMM_A_MN_MAJOR) ? 1 : 0;
+    p.b_mn = (layout & GEMM_B_MN_MAJOR) ? 1 : 0;
     p.status = plan->d_status;
     // Stream-K spreads a partial last wave over every resident unit; with
     // whole tiles only, never launch more units than tiles.
@@ -230,11 +252,20 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.trace = plan->d_trace;
 
     CUtensorMap tmA, tmB, tmC;
-    int rc = encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    // K-major operand: rows of K, box {one 128-byte row of K, rows}.  MN-major
+    // (A stored K×M, B stored K×N): rows of M or N, box {64 elements, the
+    // k-block's K rows}, several boxes per stage.
+    int rc = (layout & GEMM_A_MN_MAJOR)
+                 ? encode_2d(&tmA, dtype, A, (uint64_t)K, (uint64_t)M, (uint32_t)kbe, kMnBoxElems,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                 : encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, (uint32_t)kbe,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), (uint32_t)kbe,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        rc = (layout & GEMM_B_MN_MAJOR)
+                 ? encode_2d(&tmB, dtype, B, (uint64_t)K, (uint64_t)N, (uint32_t)kbe, kMnBoxElems,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                 : encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), (uint32_t)kbe,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
         rc = encode_2d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, 32, kChunkCols,
@@ -438,6 +469,14 @@ int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64
     int rc = validate(A, B, C, M, N, K, dtype, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int dtype, int out_dtype, int layout, void* stream) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    int rc = validate(A, B, C, M, N, K, dtype, out_dtype, layout);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream), layout);
 }
 
 int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,

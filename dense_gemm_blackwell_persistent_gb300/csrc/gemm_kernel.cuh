@@ -93,6 +93,10 @@ constexpr int kNumThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kBlockKBytes = 128;        // K bytes per k-block: one 128-byte swizzle row
 constexpr int kMmaKBytes = 32;           // K bytes of one MMA (16 bf16/f16 or 32 fp8 elements)
+// MN-major operands (A stored K×M, B stored K×N) arrive in boxes of 64
+// elements along M or N (one 128-byte row) × 64 K rows: 8 KB per box.
+constexpr int kMnBoxElems = 64;
+constexpr int kMnBoxBytes = kMnBoxElems * 128;
 constexpr int kRowsPerCta = 128;         // TMEM lanes = rows of A per CTA
 constexpr int kAccStride = 256;          // TMEM columns between the two accumulators
 constexpr int kTmemCols = 2 * kAccStride;
@@ -106,6 +110,7 @@ constexpr int kIn16 = 0, kInF8 = 1;      // operand width: bf16/f16 (kind::f16) 
 constexpr int kErrCuda = -4;      // device side: the launch's shared memory is not 1 KB aligned
 constexpr int kErrTimeout = -7;
 constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the base address
+constexpr int kRoleLayout = 10;   // status[1] for kErrCuda: an MN-major operand this tile cannot hold
 
 struct Params {
     int M, N, K;
@@ -117,6 +122,7 @@ struct Params {
     int* flags;        // stream-K: "partial published" per (split tile, CTA, epilogue warp)
     unsigned long long wait_limit_ns;   // bound on any single wait
     int stall_test;    // 1: the MMA warp waits on a barrier nothing completes (tests of the timeout path)
+    int a_mn, b_mn;    // 1: A stored K×M / B stored K×N (MN-major in shared memory)
     unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
 };
 
@@ -168,6 +174,22 @@ struct Cfg {
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
     static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // bytes landing in a pair, tracked by its leader
 };
+
+// tcgen05 shared-memory matrix descriptor for an MN-major tile written by TMA
+// with 128-byte swizzle in kMnBoxBytes boxes: each box holds 64 elements of
+// M (or N) per 128-byte row and 64 rows of K.  Swizzle atoms are 64
+// elements × 8 K rows (1 KB); the leading byte offset steps to the next 64
+// elements along M/N (the next box), the stride byte offset to the next 8
+// rows of K.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address / 16
+    d |= (uint64_t)(kMnBoxBytes >> 4) << 16;         // leading byte offset: next 64 elements of M/N
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8 rows of K
+    d |= (uint64_t)1 << 46;                          // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle
+    return d;
+}
 
 // tcgen05 shared-memory matrix descriptor for a K-major tile written by TMA
 // with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -280,6 +302,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (threadIdx.x == 0) record_error(p, kRoleSmemBase, (int)base, kErrCuda);
         return;
     }
+    // An MN-major operand needs whole 64-element boxes per CTA and 16-bit
+    // elements (a box holds the 64 K rows of a 16-bit k-block); the host only
+    // launches such tiles, and a launch that did not would otherwise wait for
+    // bytes that never come.  Uniform over the launch, before any barrier.
+    if (((p.a_mn || p.b_mn) && kIn == kInF8) || (p.a_mn && kRowsPerCta % kMnBoxElems != 0) ||
+        (p.b_mn && (C::kRowsB % kMnBoxElems != 0 || C::kRowsBLoad % kMnBoxElems != 0))) {
+        if (threadIdx.x == 0) record_error(p, kRoleLayout, kBN, kErrCuda);
+        return;
+    }
 
     const uint32_t bars = base + C::kOffBars;
     auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -378,21 +409,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
                     if (issuer) {
                         if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
-                        if constexpr (kCluster == 4) {
-                            // own A rows; a quarter of the pair-tile's B rows, written to
-                            // this CTA and to the same-rank CTA of the other pair
-                            const uint32_t fb_leader = map_shared_rank(fb, leader);
-                            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * C::kBlockKElems, a_row);
-                            tma_load_2d_pair_multicast(b_dst + pidx * C::kLoadBytesB, &tmB, fb_leader, mask,
-                                                       kb * C::kBlockKElems, b_row);
-                        } else if constexpr (kCluster == 2) {
-                            const uint32_t fb_leader = map_shared_rank(fb, leader);
-                            tma_load_2d_pair(a_dst, &tmA, fb_leader, kb * C::kBlockKElems, a_row);
-                            tma_load_2d_pair(b_dst, &tmB, fb_leader, kb * C::kBlockKElems, b_row);
+                        // Own A rows; B: this CTA's share of the tile's B rows (in a
+                        // 4-CTA unit a quarter, written to this CTA and to the
+                        // same-rank CTA of the other pair).  In a pair the copies
+                        // complete on the leader's barrier.
+                        const uint32_t fb_leader = kCluster > 1 ? map_shared_rank(fb, leader) : fb;
+                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+                        auto copy_a = [&](uint32_t dst, int x, int y) {
+                            if constexpr (kCluster > 1) tma_load_2d_pair(dst, &tmA, fb_leader, x, y);
+                            else tma_load_2d(dst, &tmA, fb, x, y);
+                        };
+                        auto copy_b = [&](uint32_t dst, int x, int y) {
+                            if constexpr (kCluster == 4) tma_load_2d_pair_multicast(dst, &tmB, fb_leader, mask, x, y);
+                            else if constexpr (kCluster == 2) tma_load_2d_pair(dst, &tmB, fb_leader, x, y);
+                            else tma_load_2d(dst, &tmB, fb, x, y);
+                        };
+                        const int kx = kb * C::kBlockKElems;
+                        const uint32_t b_q = b_dst + pidx * C::kLoadBytesB;
+                        // K-major: one box {one 128-byte row of K, rows} at (k, row).
+                        // MN-major: boxes {64 elements, 64 K rows} at (row, k).
+                        if (p.a_mn) {
+                            for (int h = 0; h < kRowsPerCta / kMnBoxElems; ++h)
+                                copy_a(a_dst + h * kMnBoxBytes, a_row + h * kMnBoxElems, kx);
                         } else {
-                            tma_load_2d(a_dst, &tmA, fb, kb * C::kBlockKElems, a_row);
-                            tma_load_2d(b_dst, &tmB, fb, kb * C::kBlockKElems, b_row);
+                            copy_a(a_dst, kx, a_row);
+                        }
+                        if (p.b_mn) {
+                            for (int h = 0; h < C::kRowsBLoad / kMnBoxElems; ++h)
+                                copy_b(b_q + h * kMnBoxBytes, b_row + h * kMnBoxElems, kx);
+                        } else {
+                            copy_b(b_q, kx, b_row);
                         }
                     }
                     __syncwarp();
@@ -414,6 +460,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (rank == 0) {
             const bool issuer = elect_one_sync();
             const uint32_t a_base = base, b_base = base + C::kOffB;
+            // Descriptor start advance per MMA (in 16-byte units): 32 bytes along
+            // a K-major row, or the MMA's K rows of 128 bytes in an MN-major tile.
+            constexpr uint32_t kStepK = kMmaKBytes >> 4;
+            constexpr uint32_t kStepMn = ((kMmaKBytes / (kIn == kInF8 ? 1 : 2)) * 128) >> 4;
+            const uint32_t a_step = p.a_mn ? kStepMn : kStepK, b_step = p.b_mn ? kStepMn : kStepK;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int i = 0;
@@ -448,15 +499,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         GEMM_TR(kTrFirstFull);
                         GEMM_TR_SET(kTrClkFirstFull, (unsigned long long)clock64());
                     }
-                    const uint64_t ad = smem_desc_sw128(a_base + stage * kStageBytesA);
-                    const uint64_t bd = smem_desc_sw128(b_base + stage * C::kStageBytesB);
+                    const uint32_t a_addr = a_base + stage * kStageBytesA, b_addr = b_base + stage * C::kStageBytesB;
+                    const uint64_t ad = p.a_mn ? smem_desc_sw128_mn(a_addr) : smem_desc_sw128(a_addr);
+                    const uint64_t bd = p.b_mn ? smem_desc_sw128_mn(b_addr) : smem_desc_sw128(b_addr);
                     const uint32_t first = kb == w.kb_begin;
                     if (issuer) {
                         tc_fence_after_sync();
 #pragma unroll
                         for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
-                            // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 in the descriptor)
-                            tc_mma<kPair, kIn == kInF8>(d_tmem, ad + 2u * j, bd + 2u * j, p.idesc, !(first && j == 0));
+                            // next 16 (bf16/f16) or 32 (fp8) elements of K: a_step / b_step above
+                            tc_mma<kPair, kIn == kInF8>(d_tmem, ad + a_step * j, bd + b_step * j, p.idesc,
+                                                        !(first && j == 0));
                         }
                         // release the slot in every CTA whose copies write into this pair's slot
                         if constexpr (kCluster == 4) tc_commit_pair(empty_bar(stage), 0xF);

@@ -77,6 +77,17 @@ typedef enum {
 
 typedef struct gemm_plan* gemm_plan_t;
 
+/* Operand storage for gemm_plan_run_layout (bit flags; 0 = the default of
+ * every other entry point: A M×K and B N×K, both K-major).
+ *   GEMM_A_MN_MAJOR: A is stored K×M row-major (a(i,k) = A[k*M + i]);
+ *   GEMM_B_MN_MAJOR: B is stored K×N row-major (b(j,k) = B[k*N + j]), i.e.
+ *                    C = A·B for a plain row-major K×N B, the layout of the
+ *                    matmuls in "Writing Mosaic GPU kernels with Pallas" and
+ *                    "Chapter 7: Writing Custom Kernels with Pallas".
+ * The tensor cores read such operands in place (MN-major shared-memory
+ * tiles); nothing is transposed in memory.  16-bit inputs only. */
+typedef enum { GEMM_K_MAJOR = 0, GEMM_A_MN_MAJOR = 1, GEMM_B_MN_MAJOR = 2 } gemm_layout_t;
+
 /* Plan options (gemm_plan_set_option).  For tuning sweeps and tests; the
  * defaults are what the library picks itself. */
 typedef enum {
@@ -126,6 +137,16 @@ int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
 /* Same, with an explicit plan.  The plan's device must be current. */
 int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M,
                   int64_t N, int64_t K, int dtype, int out_dtype, void* stream);
+
+/* C = A·Bᵀ with the operand storage of `layout` (gemm_layout_t flags).
+ * Rows of every operand must be 16-byte multiples: K for a K-major operand,
+ * M (A) or N (B) for an MN-major one.  MN-major operands need 16-bit inputs
+ * (GEMM_ERR_UNSUPPORTED for E4M3/E5M2).  With an MN-major B the tile width
+ * is limited to widths whose per-CTA share of B is a multiple of 64
+ * (GEMM_ERR_UNSUPPORTED if GEMM_OPT_TILE_N forces another).  Otherwise as
+ * gemm_plan_run. */
+int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                         int64_t K, int dtype, int out_dtype, int layout, void* stream);
 
 /* End-to-end form for callers whose operands live in host memory: copies A
  * and B (host, ideally pinned) to device buffers the plan owns (grown on

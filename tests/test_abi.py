@@ -33,7 +33,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_plan_run", "gemm_strerror"):
+    for required in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_plan_run", "gemm_strerror",
+                     "gemm_plan_run_layout"):
         assert required in names, names
 
 

@@ -313,6 +313,100 @@ def test_fp8_k_must_fill_16_bytes(g, plan):
                         64, 64, 24, g.GEMM_E4M3, g.GEMM_F32, None) == g.GEMM_ERR_UNSUPPORTED
 
 
+# ------------------------------------------------------------------ operand majors
+
+LAYOUTS = {1: "A_KxM", 2: "B_KxN", 3: "both"}
+
+
+def run_layout(g, plan, A, B, layout, out_dtype):
+    """C = A·Bᵀ with A [M,K], B [N,K] handed over in `layout`'s storage."""
+    M, K = A.shape
+    N = B.shape[0]
+    As = A.t().contiguous() if layout & 1 else A
+    Bs = B.t().contiguous() if layout & 2 else B
+    C = torch.full((M, N), float("nan"), dtype=TORCH[out_dtype], device="cuda")
+    g.gemm_plan_run_layout(plan, As.data_ptr(), Bs.data_ptr(), C.data_ptr(), M, N, K, CODE_OF[A.dtype], out_dtype,
+                           layout, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+    return C
+
+
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("layout", list(LAYOUTS), ids=list(LAYOUTS.values()))
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 264), (384, 512, 1024), (1096, 520, 136)])
+def test_operand_majors_integer_bit_exact(g, plan, unit, layout, shape):
+    """A stored K×M and/or B stored K×N, read in place (MN-major tiles):
+    integers give the oracle's bits; ragged M, N and K included."""
+    M, N, K = shape
+    configure(g, plan, unit)
+    try:
+        A, B = draw(M, N, K, dist="int", seed=70 + layout)
+        C = parity.to_f64(run_layout(g, plan, A.cuda(), B.cuda(), layout, wl.F32))
+        C_ref, _ = oracle_full(A, B)
+        assert np.array_equal(C, C_ref), f"{int((C != C_ref).sum())} mismatches"
+    finally:
+        configure(g, plan, 4)
+
+
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("layout", list(LAYOUTS), ids=list(LAYOUTS.values()))
+def test_operand_majors_random_within_tolerance(g, plan, unit, layout):
+    configure(g, plan, unit)
+    try:
+        for dtype, out in ((wl.BF16, wl.BF16), (wl.F16, wl.F16), (wl.BF16, wl.F32)):
+            A, B = draw(1000, 776, 1256, dtype=dtype, seed=80 + layout)
+            C = parity.to_f64(run_layout(g, plan, A.cuda(), B.cuda(), layout, out))
+            C_ref, S = oracle_full(A, B)
+            parity.assert_within(C, C_ref, S, out, f"layout {LAYOUTS[layout]} unit={unit} out={out}")
+    finally:
+        configure(g, plan, 4)
+
+
+def test_plain_a_times_b_full_size_sampled(g, plan):
+    """bf16 4096³ with B a plain row-major K×N matrix (C = A·B), the layout of
+    the pages' Pallas matmuls, at full size: sampled entries against the oracle."""
+    w = wl.WORKLOADS["gemm_4096_bf16"]
+    A, B = wl.make_inputs(w)                     # B drawn N×K; handed over as K×N
+    C = run_layout(g, plan, A.cuda(), B.cuda(), 2, w.out_dtype)
+    assert bool(torch.isfinite(C).all())
+    I, J = parity.sample_positions(w.M, w.N, 2048, seed=9)
+    C_ref, S = oracle.gemm_entries(wl.as_bits(A), wl.as_bits(B), w.dtype, I, J)
+    parity.assert_within(parity.to_f64(C)[I, J], C_ref, S, w.out_dtype, "A·B, B K×N")
+
+
+def test_matmul_helper_operand_majors(g, plan):
+    A, B = draw(264, 328, 200, seed=91)
+    Ad, Bd = A.cuda(), B.cuda()
+    C_ref, S = oracle_full(A, B)
+    Akm, Bkn = Ad.t().contiguous(), Bd.t().contiguous()
+    for kw, a, b in (({"b_kn": True}, Ad, Bkn), ({"a_km": True}, Akm, Bd), ({"a_km": True, "b_kn": True}, Akm, Bkn)):
+        C = g.matmul(a, b, out_dtype=torch.float32, plan=plan, **kw)
+        torch.cuda.synchronize()
+        parity.assert_within(parity.to_f64(C), C_ref, S, wl.F32, str(kw))
+
+
+def test_operand_major_rules(g, plan):
+    import ctypes
+    vp = ctypes.c_void_p
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    args = (vp(plan), vp(A.data_ptr()), vp(A.data_ptr()), vp(C.data_ptr()))
+    rs = g.raw_status
+    assert rs("gemm_plan_run_layout", *args, 64, 64, 64, 0, 2, 4, None) == g.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_run_layout", *args, 64, 64, 64, 3, 2, 1, None) == g.GEMM_ERR_UNSUPPORTED  # fp8
+    assert rs("gemm_plan_run_layout", *args, 60, 64, 64, 0, 2, 1, None) == g.GEMM_ERR_UNSUPPORTED  # M*2 % 16
+    assert rs("gemm_plan_run_layout", *args, 64, 64, 60, 0, 2, 3, None) == g.GEMM_OK   # K free when both MN-major
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+    fresh = g.gemm_plan_create(0)
+    try:
+        g.gemm_plan_set_option(fresh, g.GEMM_OPT_TILE_N, 224)      # a 112-row B share: not whole boxes
+        assert rs("gemm_plan_run_layout", vp(fresh), *args[1:], 64, 64, 64, 0, 2, 2, None) == g.GEMM_ERR_UNSUPPORTED
+    finally:
+        g.gemm_plan_destroy(fresh)
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16",
