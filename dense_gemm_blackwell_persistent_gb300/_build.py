@@ -1,8 +1,9 @@
 """Build the CUDA library in-tree with nvcc (sm_103a only).
 
 Produces ``dense_gemm_blackwell_persistent_gb300/_lib/libgb300gemm.so`` from
-``csrc/gemm_api.cu`` (host side) and eighteen objects of ``csrc/kernels_inst.cu``
-(one per unit size × output type × operand width), compiled in parallel.  The CUDA
+``csrc/gemm_api.cu`` (host side) and 24 objects of ``csrc/kernels_inst.cu``
+(one per unit size × output type × operand width, plus the padded MN-major-B
+forms), compiled in parallel.  The CUDA
 runtime is linked statically and the driver's tensor-map encoder is looked up
 at run time, so the library loads on a machine without a GPU.
 """
@@ -59,7 +60,8 @@ def up_to_date(variant: str = "") -> bool:
 
 # (CTAs per unit, output type, operand width) variants of the kernel, one
 # object file each
-VARIANTS = [(cluster, out, inp) for cluster in (1, 2, 4) for out in (0, 1, 2) for inp in (0, 1)]
+VARIANTS = [(cluster, out, inp, 0) for cluster in (1, 2, 4) for out in (0, 1, 2) for inp in (0, 1)]
+VARIANTS += [(cluster, out, 0, 1) for cluster in (1, 2) for out in (0, 1, 2)]   # padded MN-major B
 
 
 def _compile(args):
@@ -85,10 +87,10 @@ def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
     if verbose:
         common.insert(1, "-Xptxas=-v")
     jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose)]
-    for cluster, out, inp in VARIANTS:
-        obj = os.path.join(objdir, f"kernels_c{cluster}_o{out}_i{inp}.o")
+    for cluster, out, inp, pad in VARIANTS:
+        obj = os.path.join(objdir, f"kernels_c{cluster}_o{out}_i{inp}_p{pad}.o")
         jobs.append((common + [f"-DGEMM_INST_CLUSTER={cluster}", f"-DGEMM_INST_OUT={out}", f"-DGEMM_INST_IN={inp}",
-                               os.path.join(CSRC, "kernels_inst.cu"), "-o", obj], verbose))
+                               f"-DGEMM_INST_BMN={pad}", os.path.join(CSRC, "kernels_inst.cu"), "-o", obj], verbose))
     workers = max(1, min(len(jobs), os.cpu_count() or 1))
     with ThreadPoolExecutor(workers) as ex:
         logs = list(ex.map(_compile, jobs))

@@ -182,12 +182,16 @@ int resident_units(const gemm_plan* plan, int cluster) {
 // BN + 48 (316 / 242 / 183 ns for BN = 256 / 192 / 128 with CTA pairs at
 // 8192³), so a narrower tile pays off when it fills the last wave: 224 at
 // 4096³ (4 full waves instead of 3.4) and at 1024×4096×4096.
-// A tile width an MN-major B can use: every CTA's share of the tile's B
-// rows, as held for the MMA and as loaded, whole 64-element TMA boxes.
-bool width_fits_layout(int bn, int cluster, int layout) {
-    if (!(layout & GEMM_B_MN_MAJOR)) return true;
+// With an MN-major B, whether every CTA's share of the tile's B rows (as
+// held for the MMA and as loaded) is whole 64-element TMA boxes.  If not, a
+// 1- or 2-CTA unit uses the padded kernel form (shares rounded up to whole
+// boxes); a 4-CTA unit cannot.
+bool b_boxes_exact(int bn, int cluster) {
     const int pair = cluster >= 2 ? 2 : 1;
     return (bn / pair) % kMnBoxElems == 0 && (bn / cluster) % kMnBoxElems == 0;
+}
+bool width_fits_layout(int bn, int cluster, int layout) {
+    return !(layout & GEMM_B_MN_MAJOR) || cluster <= 2 || b_boxes_exact(bn, cluster);
 }
 
 // Returns 0 when no width fits (a forced width the layout cannot use).
@@ -222,7 +226,8 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     const int cluster = unit_ctas(plan, K, dtype, layout);
     const int bn = choose_tile_n(plan, M, N, cluster, layout);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
-    const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0);
+    const bool pad = (layout & GEMM_B_MN_MAJOR) && !b_boxes_exact(bn, cluster);
+    const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0, pad);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * cluster;
     Params p;
@@ -327,9 +332,9 @@ size_t trace_bytes(const gemm_plan* plan) {
 int query_capacity(gemm_plan* plan, int cluster) {
     int max_smem = 0;
     KernelFn probe = nullptr;
-    for (int v = 0; v < 6; ++v) {   // output type × operand width
+    for (int v = 0; v < 9; ++v) {   // output type × (operand width, or the padded MN-major-B form)
         for (int i = 0; i < kNumTileWidths; ++i) {
-            const KernelInfo ki = kernel_info(cluster, kTileWidths[i], v % 3, v / 3);
+            const KernelInfo ki = kernel_info(cluster, kTileWidths[i], v % 3, v / 3 == 1 ? 1 : 0, v / 3 == 2);
             if (ki.fn == nullptr) continue;
             if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem_bytes) !=
                 cudaSuccess) {

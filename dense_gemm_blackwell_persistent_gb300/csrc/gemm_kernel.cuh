@@ -138,8 +138,11 @@ constexpr int kFixupBytes = kPartialFloats * 4;   // shared memory per epilogue 
 // columns, a multiple of 32 up to 256).  kOut: C element type.  kIn:
 // operand width; a k-block is one 128-byte swizzle row of K either way
 // (64 bf16/f16 or 128 fp8 elements), so shared-memory layout, descriptors
-// and the ring are the same for both.
-template <int kCluster, int kBN, int kOut, int kIn>
+// and the ring are the same for both.  kBMnPad: B is MN-major and a CTA's
+// share of it is rounded up to whole 64-element boxes in shared memory (the
+// extra rows are loaded but never read by the MMA), for tile widths whose
+// share is not a multiple of 64 (e.g. 112 rows of a 256×224 pair tile).
+template <int kCluster, int kBN, int kOut, int kIn, bool kBMnPad = false>
 struct Cfg {
     static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "1, 2 or 4 CTAs per unit");
     static_assert(kBN % 32 == 0 && kBN >= 64 && kBN <= 256, "tile width");
@@ -150,8 +153,10 @@ struct Cfg {
     static constexpr int kRowsBLoad = kBN / kCluster;             // B rows each CTA loads
     static_assert(kRowsBLoad % 8 == 0, "B boxes must fill 1 KB swizzle atoms");
     static constexpr int kBlockKElems = kIn == kInF8 ? kBlockKBytes : kBlockKBytes / 2;   // TMA K coordinate step
-    static constexpr int kStageBytesB = kRowsB * kBlockKBytes;
-    static constexpr int kLoadBytesB = kRowsBLoad * kBlockKBytes;
+    static_assert(!kBMnPad || (kCluster <= 2 && kIn == kIn16), "padded MN-major B: 1- or 2-CTA units, 16-bit");
+    static constexpr int kBoxesB = (kRowsBLoad + kMnBoxElems - 1) / kMnBoxElems;   // MN-major B boxes per load
+    static constexpr int kStageBytesB = kBMnPad ? kBoxesB * kMnBoxBytes : kRowsB * kBlockKBytes;
+    static constexpr int kLoadBytesB = kBMnPad ? kBoxesB * kMnBoxBytes : kRowsBLoad * kBlockKBytes;
     static constexpr int kStageBytes = kStageBytesA + kStageBytesB;
     static constexpr int kOutBytes = kOut == kOutF32 ? 4 : 2;
     static constexpr int kRowBytes = kChunkCols * kOutBytes;    // 128 (fp32) or 64 (16-bit)
@@ -279,11 +284,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int out) {
     }
 }
 
-template <int kCluster, int kBN, int kOut, int kIn>
+template <int kCluster, int kBN, int kOut, int kIn, bool kBMnPad>
 __global__ void __launch_bounds__(kNumThreads, 1)
     gemm_tn_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const Params p) {
-    using C = Cfg<kCluster, kBN, kOut, kIn>;
+    using C = Cfg<kCluster, kBN, kOut, kIn, kBMnPad>;
     constexpr int kPair = C::kPair;
     constexpr int kStages = C::kStages;
     constexpr int kChunks = kBN / kChunkCols;
@@ -307,7 +312,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // launches such tiles, and a launch that did not would otherwise wait for
     // bytes that never come.  Uniform over the launch, before any barrier.
     if (((p.a_mn || p.b_mn) && kIn == kInF8) || (p.a_mn && kRowsPerCta % kMnBoxElems != 0) ||
-        (p.b_mn && (C::kRowsB % kMnBoxElems != 0 || C::kRowsBLoad % kMnBoxElems != 0))) {
+        (kBMnPad && !p.b_mn) ||
+        (p.b_mn && !kBMnPad && (C::kRowsB % kMnBoxElems != 0 || C::kRowsBLoad % kMnBoxElems != 0))) {
         if (threadIdx.x == 0) record_error(p, kRoleLayout, kBN, kErrCuda);
         return;
     }
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             copy_a(a_dst, kx, a_row);
                         }
                         if (p.b_mn) {
-                            for (int h = 0; h < C::kRowsBLoad / kMnBoxElems; ++h)
+                            for (int h = 0; h < C::kBoxesB; ++h)
                                 copy_b(b_q + h * kMnBoxBytes, b_row + h * kMnBoxElems, kx);
                         } else {
                             copy_b(b_q, kx, b_row);

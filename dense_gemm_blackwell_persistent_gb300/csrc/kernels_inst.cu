@@ -1,7 +1,9 @@
 // kernels_inst.cu -- instantiates gemm_tn_persistent for one unit size
 // (GEMM_INST_CLUSTER = 1, 2 or 4 CTAs), one output type (GEMM_INST_OUT =
-// 0 bf16, 1 f16, 2 fp32) and one operand width (GEMM_INST_IN = 0 bf16/f16,
-// 1 E4M3/E5M2) over every tile width of kernel_table.h.  The build compiles
+// 0 bf16, 1 f16, 2 fp32), one operand width (GEMM_INST_IN = 0 bf16/f16,
+// 1 E4M3/E5M2) and, with GEMM_INST_BMN = 1, the padded MN-major-B form
+// (1- and 2-CTA units, 16-bit operands), over every tile width of
+// kernel_table.h.  The build compiles
 // this file once per combination, in parallel.
 #include "gemm_kernel.cuh"
 #include "kernel_table.h"
@@ -15,18 +17,21 @@
 #ifndef GEMM_INST_IN
 #error "GEMM_INST_IN must be defined"
 #endif
+#ifndef GEMM_INST_BMN
+#define GEMM_INST_BMN 0   // 1: the padded MN-major-B variants (see Cfg::kBMnPad)
+#endif
 
-#define GEMM_CAT2(a, b, c) kernel_info_c##a##_o##b##_i##c
-#define GEMM_CAT(a, b, c) GEMM_CAT2(a, b, c)
-#define GEMM_INFO_FN GEMM_CAT(GEMM_INST_CLUSTER, GEMM_INST_OUT, GEMM_INST_IN)
+#define GEMM_CAT2(a, b, c, d) kernel_info_c##a##_o##b##_i##c##_p##d
+#define GEMM_CAT(a, b, c, d) GEMM_CAT2(a, b, c, d)
+#define GEMM_INFO_FN GEMM_CAT(GEMM_INST_CLUSTER, GEMM_INST_OUT, GEMM_INST_IN, GEMM_INST_BMN)
 
 namespace gb300 {
 
 template <int kBN>
 static KernelInfo make_info() {
-    using C = Cfg<GEMM_INST_CLUSTER, kBN, GEMM_INST_OUT, GEMM_INST_IN>;
-    return KernelInfo{gemm_tn_persistent<GEMM_INST_CLUSTER, kBN, GEMM_INST_OUT, GEMM_INST_IN>, C::kSmemBytes,
-                      C::kStages};
+    using C = Cfg<GEMM_INST_CLUSTER, kBN, GEMM_INST_OUT, GEMM_INST_IN, GEMM_INST_BMN != 0>;
+    return KernelInfo{gemm_tn_persistent<GEMM_INST_CLUSTER, kBN, GEMM_INST_OUT, GEMM_INST_IN, GEMM_INST_BMN != 0>,
+                      C::kSmemBytes, C::kStages};
 }
 
 KernelInfo GEMM_INFO_FN(int bn) {

@@ -141,10 +141,10 @@ int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64
 /* C = A·Bᵀ with the operand storage of `layout` (gemm_layout_t flags).
  * Rows of every operand must be 16-byte multiples: K for a K-major operand,
  * M (A) or N (B) for an MN-major one.  MN-major operands need 16-bit inputs
- * (GEMM_ERR_UNSUPPORTED for E4M3/E5M2).  With an MN-major B the tile width
- * is limited to widths whose per-CTA share of B is a multiple of 64
- * (GEMM_ERR_UNSUPPORTED if GEMM_OPT_TILE_N forces another).  Otherwise as
- * gemm_plan_run. */
+ * (GEMM_ERR_UNSUPPORTED for E4M3/E5M2).  With an MN-major B, a 4-CTA
+ * multicast unit (GEMM_OPT_MULTICAST = 1) needs tile width 256
+ * (GEMM_ERR_UNSUPPORTED if GEMM_OPT_TILE_N forces another); 1- and 2-CTA
+ * units take every width.  Otherwise as gemm_plan_run. */
 int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M, int64_t N,
                          int64_t K, int dtype, int out_dtype, int layout, void* stream);
 

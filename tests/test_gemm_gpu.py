@@ -401,10 +401,30 @@ def test_operand_major_rules(g, plan):
     assert g.gemm_plan_status(plan) == 0
     fresh = g.gemm_plan_create(0)
     try:
-        g.gemm_plan_set_option(fresh, g.GEMM_OPT_TILE_N, 224)      # a 112-row B share: not whole boxes
+        # a 4-CTA unit loads a 56-row quarter of a 224-wide B tile: not whole boxes
+        g.gemm_plan_set_option(fresh, g.GEMM_OPT_TILE_N, 224)
+        g.gemm_plan_set_option(fresh, g.GEMM_OPT_MULTICAST, 1)
         assert rs("gemm_plan_run_layout", vp(fresh), *args[1:], 64, 64, 64, 0, 2, 2, None) == g.GEMM_ERR_UNSUPPORTED
     finally:
         g.gemm_plan_destroy(fresh)
+
+
+@pytest.mark.parametrize("unit", [2, 1])
+@pytest.mark.parametrize("tile_n", TILE_NS)
+@pytest.mark.parametrize("layout", [2, 3], ids=["B_KxN", "both"])
+def test_operand_major_b_every_tile_width(g, fresh_plan, unit, tile_n, layout):
+    """An MN-major B at every tile width; where a CTA's share of B is not whole
+    64-element boxes (e.g. 112 rows of a 256×224 pair tile) the padded kernel
+    form loads whole boxes and the MMA reads only the share."""
+    configure(g, fresh_plan, unit)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, tile_n)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MAX_CTAS, 8)   # several tiles per unit
+    M, N, K = 600, 1000, 392
+    A, B = draw(M, N, K, dist="int", seed=95 + tile_n)
+    C = parity.to_f64(run_layout(g, fresh_plan, A.cuda(), B.cuda(), layout, wl.F32))
+    assert g.gemm_plan_last_tile_n(fresh_plan) == tile_n
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(C, C_ref), f"{int((C != C_ref).sum())} mismatches"
 
 
 # ------------------------------------------------------------------ full-size workloads
