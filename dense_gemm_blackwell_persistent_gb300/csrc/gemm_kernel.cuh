@@ -176,6 +176,8 @@ struct Cfg {
     static_assert((2 * kStages + 4 + kEpiWarps) * 8 <= kBarBytes, "barrier area");
     static constexpr uint32_t kPartialBytes = kBN * 32 * 4;   // one epilogue warp's fp32 partial
     static_assert(kEpiWarps * kFixupBytes <= kOffStaging, "fix-up buffers must fit in the operand ring");
+    static_assert(kEpiWarps * (kBN / kChunkCols) * kSlotBytes <= kOffStaging,
+                  "the last tile's store boxes must fit in the operand ring");
     static_assert(kStageBytesA % 1024 == 0 && kStageBytesB % 1024 == 0, "1 KB aligned tiles");
     static constexpr uint32_t kTxBytes = kStageBytes * kPair;   // bytes landing in a pair, tracked by its leader
 };
@@ -552,13 +554,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t staging = base + C::kOffStaging + (uint32_t)(warp - 2) * 2u * C::kSlotBytes;
         uint32_t slot = 0;
 
-        // Convert one 32-column chunk (fp32 values of this thread's row),
-        // stage it swizzled and TMA-store it to C at (ccol, row0).
-        auto store_chunk = [&](const uint32_t (&cur)[32], int ccol, int row0) {
-            const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
-            ++slot;
-            if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
-            __syncwarp();
+        // Convert one 32-column chunk (fp32 values of this thread's row) and
+        // write it swizzled into the 32-row store box at `buf`.
+        auto stage_chunk = [&](uint32_t buf, const uint32_t (&cur)[32]) {
             const uint32_t row_addr = buf + (uint32_t)lane * C::kRowBytes;
             if constexpr (kOut == kOutF32) {
                 // 128-byte rows: 16-byte chunk q stored at q ^ (row % 8)
@@ -577,6 +575,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     st_shared_v4(row_addr + (((uint32_t)q ^ (((uint32_t)lane >> 1) & 3u)) << 4), w0, w1, w2, w3);
                 }
             }
+        };
+        // Stage one chunk in this warp's two staging boxes and TMA-store it to
+        // C at (ccol, row0).
+        auto store_chunk = [&](const uint32_t (&cur)[32], int ccol, int row0) {
+            const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
+            ++slot;
+            if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
+            __syncwarp();
+            stage_chunk(buf, cur);
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
@@ -598,7 +605,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int row0 = mt * C::kTileM + (int)crank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
-            if (w.ncontrib == 1) {
+            if (w.ncontrib == 1 && i == nwork - 1) {
+                // The unit's last tile: nothing overlaps its epilogue, and its
+                // operand ring is idle (no later loads, every MMA done), so each
+                // chunk gets its own box there, one fence covers them all and
+                // the stores go out back to back.
+                if (row0 < p.M) {
+                    const uint32_t region = base + (uint32_t)(warp - 2) * (uint32_t)(kChunks * C::kSlotBytes);
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(t_row, ra);
+                    tmem_ld_wait(ra);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+                        uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+                        if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
+                        stage_chunk(region + (uint32_t)(c * C::kSlotBytes), cur);
+                        if (c + 1 < kChunks) tmem_ld_wait(nxt);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        for (int c = 0; c < kChunks && col0 + c * kChunkCols < p.N; ++c)
+                            tma_store_2d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (w.ncontrib == 1) {
                 if (row0 < p.M) {
                     // Two register sets: the TMEM load of chunk c+1 is in flight
                     // while chunk c is converted, staged and stored.
