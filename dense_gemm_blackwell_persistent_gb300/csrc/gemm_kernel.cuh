@@ -62,7 +62,7 @@ namespace gb300 {
 // Optional timeline tracing (build with -DGEMM_TRACE): per-CTA
 // %globaltimer stamps and wait totals in a device buffer of kTraceSlots
 // 64-bit words per CTA.  Without GEMM_TRACE the macros compile to nothing.
-constexpr int kTraceSlots = 64;
+constexpr int kTraceSlots = 80;
 enum TraceSlot {
     kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrFirstFull = 3, kTrTeardown = 4, kTrExit = 5,
     kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8, kTrWorkItems = 9,
@@ -76,13 +76,28 @@ enum TraceSlot {
     kTrReduceDone = 48,   // + item: stream-K reduction finished (last contributor)
     kTrClkFirstFull = 15, // SM clock cycles (clock64) at first_full ...
     kTrClkMmaEnd = 56,    // ... and at mma_end + item: cycles per k-block
+    kTrClkPro = 64,       // + 0..8: SM cycles at the prologue steps (see timeline.PROLOGUE)
 };
 #ifdef GEMM_TRACE
 #define GEMM_TR(slot) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
 #define GEMM_TR_ITEM(base, item) do { if ((item) < 8) GEMM_TR((base) + (item)); } while (0)
 #define GEMM_TR_SET(slot, v) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = (v); } while (0)
 #define GEMM_TR_NOW() global_timer_ns()
+// Prologue cycle stamps stay in registers (constant indices) until the
+// teardown writes them, so that taking them costs a few cycles and no
+// memory traffic; the %globaltimer points above are too heavy for steps of
+// a few hundred cycles.
+#define GEMM_TR_CLK(step) (tr_clk[(step)] = (unsigned long long)clock64())
+#define GEMM_TR_CLK_FLUSH()                                                            \
+    do {                                                                               \
+        if (p.trace)                                                                   \
+            for (int s_ = 0; s_ < 9; ++s_)                                             \
+                if (tr_clk[s_]) p.trace[blockIdx.x * kTraceSlots + kTrClkPro + s_] = tr_clk[s_]; \
+        if (p.trace && tr_entry_ns) p.trace[blockIdx.x * kTraceSlots + kTrEntry] = tr_entry_ns;      \
+    } while (0)
 #else
+#define GEMM_TR_CLK_FLUSH() do { } while (0)
+#define GEMM_TR_CLK(step) do { } while (0)
 #define GEMM_TR(slot) do { } while (0)
 #define GEMM_TR_ITEM(base, item) do { } while (0)
 #define GEMM_TR_SET(slot, v) do { } while (0)
@@ -113,11 +128,13 @@ constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the bas
 constexpr int kRoleLayout = 10;   // status[1] for kErrCuda: an MN-major operand this tile cannot hold
 
 struct Params {
-    int M, N, K;
-    int tiles_m, tiles_n, k_blocks, num_tiles, group_m;
+    // What decoding a work item reads comes first, so that it shares one
+    // constant-cache line.
+    Schedule sched;    // whole-tile waves + stream-K part
+    int tiles_m, tiles_n, group_m, k_blocks;
+    int M, N, K, num_tiles;
     uint32_t idesc;
     int* status;       // [0] first error code, [1] role, [2] block, [3] detail
-    Schedule sched;    // whole-tile waves + stream-K part
     float* partials;   // stream-K: one partial-tile slot per unit, or null
     int* flags;        // stream-K: "partial published" per (split tile, CTA, epilogue warp)
     unsigned long long wait_limit_ns;   // bound on any single wait
@@ -302,7 +319,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // misaligned all of them would record the error and return here,
     // before touching any barrier, TMEM or cluster peer.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    if (threadIdx.x == 0) GEMM_TR(kTrEntry);
+#ifdef GEMM_TRACE
+    unsigned long long tr_clk[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    unsigned long long tr_entry_ns = 0;
+    if (threadIdx.x == 0) {
+        GEMM_TR_CLK(0);
+        tr_entry_ns = global_timer_ns();
+    }
+#endif
     const uint32_t base = smem_addr(smem_raw);
     uint8_t* smem = smem_raw;
     if (base & 1023u) {
@@ -358,11 +382,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(fix_bar(e), 1);
         *abort_flag = 0;
         fence_mbar_init_cluster();
+        GEMM_TR_CLK(1);
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
         prefetch_tensormap(&tmC);
+        GEMM_TR_CLK(2);
     }
     // The barrier inits are published CTA-wide and to the peer CTAs by the
     // cluster barrier (a CTA barrier without a cluster).  The MMA warp
@@ -371,19 +397,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // the epilogue warps through a named barrier of warps 1-5.
     if constexpr (kCluster > 1) cluster_arrive();
     else __syncthreads();
+    if (threadIdx.x == 0) GEMM_TR_CLK(3);
     if (warp == 1) {
         tmem_alloc<kPair>(smem_addr(tmem_holder), kTmemCols);
         tmem_relinquish<kPair>();
     }
     if constexpr (kCluster > 1) cluster_wait();
+    if (threadIdx.x == 0) GEMM_TR_CLK(4);
     uint32_t tmem_base = 0;
     if (warp >= 1) {
         tc_fence_before_sync();
         named_bar_sync(1, kNumThreads - 32);
         tc_fence_after_sync();
         tmem_base = *tmem_holder;
+        if (warp == 1 && lane == 0) GEMM_TR_CLK(8);
     }
-    if (threadIdx.x == 0) GEMM_TR(kTrSetup);
 
     // The producer and MMA loops run on the whole warp, so that stage, phase
     // and the descriptors stay warp-uniform (the TMA and tcgen05.mma operands
@@ -402,7 +430,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const Work w = work_item(p.sched, pair_id, j);
                 int a_row, b_row;
                 operand_rows(w.tile, a_row, b_row);
-                if (j == 0 && lane == 0) GEMM_TR(kTrFirstItem);
+                if (j == 0 && lane == 0) GEMM_TR_CLK(5);
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tw = GEMM_TR_NOW();
                     if (!__all_sync(0xffffffffu,
@@ -411,7 +439,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     empty_wait_ns += GEMM_TR_NOW() - tw;
-                    if (j == 0 && kb == w.kb_begin) GEMM_TR(kTrFirstLoad);
+                    if (j == 0 && kb == w.kb_begin && lane == 0) GEMM_TR_CLK(6);
                     const uint32_t fb = full_bar(stage);
                     const uint32_t a_dst = base + stage * kStageBytesA;
                     const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
@@ -448,6 +476,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         } else {
                             copy_b(b_q, kx, b_row);
                         }
+                        if (j == 0 && kb == w.kb_begin) GEMM_TR_CLK(7);
                     }
                     __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -757,6 +786,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (lane == 0) GEMM_TR(kTrDealloc);
     }
     if (threadIdx.x == 0) GEMM_TR(kTrExit);
+    if (lane == 0 && warp <= 1) GEMM_TR_CLK_FLUSH();
 }
 
 }  // namespace gb300

@@ -26,11 +26,12 @@ from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_MULTICAST, GEMM_OP
                gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_last_launch, gemm_plan_run,
                gemm_plan_set_option, gemm_plan_trace)
 
-POINTS = {0: "entry", 1: "setup_done", 10: "first_item_decoded", 2: "first_load_issued", 3: "first_full",
-          11: "epilogue_stores_done", 4: "teardown", 12: "cluster_arrived", 13: "cluster_done", 14: "tmem_dealloc",
-          5: "exit"}
+POINTS = {0: "entry", 3: "first_full", 11: "epilogue_stores_done", 4: "teardown", 12: "cluster_arrived",
+          13: "cluster_done", 14: "tmem_dealloc", 5: "exit"}
 ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published", 48: "reduce_done"}
 TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us"}
+PROLOGUE = {1: "barriers_initialised", 2: "tensormaps_prefetched", 3: "cluster_arrived", 4: "cluster_passed",
+            5: "first_item_decoded", 6: "first_slot_free", 7: "first_loads_issued", 8: "mma_warp_has_tmem"}
 
 
 def summarise(buf: np.ndarray, ctas: int) -> dict:
@@ -68,6 +69,16 @@ def summarise(buf: np.ndarray, ctas: int) -> dict:
             mhz = (cj[ok] - c0[ok]) / np.maximum(nj[ok] - n0[ok], 1) * 1e3
             out[f"sm_mhz_to_mma_end[{j}]"] = round(float(np.median(mhz)), 1)
             out[f"cycles_first_full_to_mma_end[{j}]"] = int(np.median(cj[ok] - c0[ok]))
+    # SM cycles of the prologue steps, relative to the CTA's entry stamp
+    c0 = t[:, 64]
+    have = c0 > 0
+    if have.any():
+        for k, name in PROLOGUE.items():
+            v = t[have, 64 + k]
+            ok = v > 0
+            if ok.any():
+                d = (v[ok] - c0[have][ok]).astype(np.int64)
+                out[f"cycles_to_{name}"] = [int(d.min()), int(np.median(d)), int(d.max()), int(ok.sum())]
     for col, name in TOTALS.items():
         v = t[:, col][t[:, col] > 0] / 1e3
         if v.size:
