@@ -370,7 +370,7 @@ def main():
         e2e = {"value": e2e_value, "unit": "TFLOP/s",
                "h2d_bytes_per_step": (w.M + w.N) * w.K * wl.ELEM_BYTES[w.dtype],
                "d2h_bytes_per_step": w.M * w.N * wl.ELEM_BYTES[w.out_dtype],
-               "how": "gemm_plan_run_host: pinned host A,B in, host C out, copies + kernel + sync per step, "
+               "how": "gemm_plan_run_host: pinned host A,B in, host C out, row chunks with copies in, products and copies back overlapped on the plan's streams, sync per step, "
                       f"host wall clock, {args.e2e_steps} steps"}
 
     cpu = None

@@ -151,7 +151,9 @@ int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C
 /* End-to-end form for callers whose operands live in host memory: copies A
  * and B (host, ideally pinned) to device buffers the plan owns (grown on
  * demand and kept for reuse), runs the product, copies C back to host
- * memory, and synchronises `stream` before returning.  Same shape rules. */
+ * memory, and synchronises `stream` before returning.  Copies and products
+ * overlap on streams the plan owns (A and C in row chunks), ordered after
+ * the work already on `stream`.  Same shape rules. */
 int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host, void* C_host,
                        int64_t M, int64_t N, int64_t K, int dtype, int out_dtype, void* stream);
 

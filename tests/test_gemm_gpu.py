@@ -571,6 +571,25 @@ def test_implicit_plan_and_host_entry_agree(g, plan):
     assert torch.equal(C1.cpu().view(torch.int16), C3.view(torch.int16))
 
 
+@pytest.mark.parametrize("shape", [(2100, 520, 264), (1024, 776, 392), (4096, 264, 136)])
+def test_host_entry_pipelined_chunks(g, fresh_plan, shape):
+    """gemm_plan_run_host splits A into row chunks (copies, products and
+    copies back overlapped on the plan's streams): integer inputs give the
+    oracle's bits for every chunk, including a ragged last one, and the
+    caller's stream sees the finished C."""
+    M, N, K = shape
+    A, B = draw(M, N, K, dist="int", seed=M + N)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    for out in (wl.F32, wl.BF16):
+        Ch = torch.full((M, N), float("nan"), dtype=TORCH[out]).pin_memory()
+        g.gemm_plan_run_host(fresh_plan, Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), M, N, K, wl.BF16, out,
+                             torch.cuda.current_stream().cuda_stream)
+        assert g.gemm_plan_status(fresh_plan) == 0
+        C_ref, _ = oracle_full(A, B)
+        want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(parity.to_f64(Ch), want), f"{shape} out={out}"
+
+
 def test_deterministic(g, plan):
     w = wl.WORKLOADS["gemm_1024x4096x4096_f16"]
     A, B = wl.make_inputs(w)
