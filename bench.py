@@ -99,25 +99,38 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# Device-side sources: what a launch of the kernel executes.  The host side
+# (gemm_api.cu) only chooses the launch shape, which traffic records carry
+# separately.
+DEVICE_SOURCES = ("gemm_kernel.cuh", "kernel_table.h", "kernels_inst.cu", "ptx.cuh", "schedule.h")
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DEVICE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def launch_key(launch: dict) -> str:
+    return " ".join(f"{k}={launch[k]}" for k in ("ctas", "ctas_per_unit", "tile_n", "dp_waves", "sk_tiles"))
+
+
+def recorded_traffic(workload: str, launch: dict = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its digest line must match); else None."""
+    the current device code (its digest line must match) and, when `launch`
+    is given, with the same launch shape; else None."""
     path = os.path.join(ROOT, "profiles", f"traffic_{KERNEL_NAME}_{workload}.txt")
     try:
         fields = dict(line.split(":", 1) for line in open(path) if ":" in line and not line.startswith("#"))
     except OSError:
         return None
     if fields.get("source_digest", "").strip() != source_digest():
+        return None
+    if launch is not None and fields.get("launch", "").strip() != launch_key(launch):
         return None
     try:
         return int(fields["dram_bytes_per_launch"].strip())
@@ -321,7 +334,7 @@ def main():
         # no measured fp8 figure: the bf16 one times the nominal dense ratio 4.5 / 2.25
         peak *= 2.0
         peak_note += " x 2 (nominal fp8:bf16 dense ratio)"
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, g.gemm_plan_last_launch(plan))
 
     extra = {}
     ref_call, ref_how = None, None
