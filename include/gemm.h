@@ -97,9 +97,14 @@ typedef enum {
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
     GEMM_OPT_TILE_N = 4,         /* tile width: 256, 224, 192, 160 or 128 (0 = default:
                                     chosen per problem to fill whole waves)             */
-    GEMM_OPT_STREAM_K = 5,       /* 1: spread the K work of a partial last wave over all
-                                    resident units (stream-K tail, deterministic
-                                    fixup); 0 (default): whole tiles only              */
+    GEMM_OPT_STREAM_K = 5,       /* 1: spread the K work of the last whole wave and a
+                                    partial one over all resident units in ranges
+                                    longer than a tile (a tile is split at most two
+                                    ways; deterministic fix-up), or halve the tiles
+                                    along K when there are fewer than half as many
+                                    tiles as units, where that is predicted to pay;
+                                    runs that may overlap on the GPU then need
+                                    separate plans.  0 (default): whole tiles only     */
     GEMM_OPT_MULTICAST = 6,      /* with CTA pairs: 1 = two pairs per 4-CTA cluster work
                                     on vertically adjacent tiles and share their B tile
                                     through TMA multicast (512×BN per cluster); 0 = one
@@ -118,8 +123,8 @@ typedef enum {
  * gemm_run() uses on that device while it is the newest one alive.  Queries
  * the SM count and the resident cluster capacity, sets kernel attributes and
  * allocates the plan's device memory: a 16-byte status record and the
- * stream-K workspace (256 KB of fp32 partials per SM, about 40 MB on GB300,
- * plus a few KB of counters).  `flags` must be 0.  The caller owns the plan
+ * stream-K workspace (128 KB of fp32 partials per SM, about 19.5 MB on GB300,
+ * plus a few KB of flags).  `flags` must be 0.  The caller owns the plan
  * and frees it with gemm_plan_destroy(). */
 int gemm_plan_create(gemm_plan_t* plan, int device, unsigned flags);
 
@@ -159,7 +164,7 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
 
 /* Read and clear the plan's device status word.  Synchronises the device.
  * *device_status receives GEMM_OK or the first device-side error code
- * recorded since the last call; after an error the stream-K counters are
+ * recorded since the last call; after an error the stream-K flags are
  * reset too, so the plan can be used again. */
 int gemm_plan_status(gemm_plan_t plan, int* device_status);
 
@@ -179,8 +184,9 @@ int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* 
  * builds return GEMM_ERR_UNSUPPORTED after filling *ctas and *slots).  Copies
  * *ctas × *slots 64-bit words to `host` (at least that many bytes) and
  * clears the device buffer; synchronises the device.  Word s of CTA c is a
- * %globaltimer stamp in ns (or a wait total) at trace point s; see
- * TraceSlot in the kernel source. */
+ * %globaltimer stamp in ns, a wait total in ns, or an SM cycle count (the
+ * prologue steps and the MMA warp's per-tile stamps), per TraceSlot in the
+ * kernel source. */
 int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* slots);
 
 /* Free the plan.  The caller must have synchronised every stream that still
