@@ -459,6 +459,22 @@ def test_medium_ragged_full(g, plan):
 
 # ------------------------------------------------------------------ edges and API behaviour
 
+@pytest.mark.parametrize("unit", UNITS)
+def test_long_k(g, plan, unit):
+    """A K loop of 512 k-blocks (K = 32768) through a ring of 6-7 slots: the
+    barrier phases wrap ~75 times.  Integer inputs keep every partial sum
+    exact in fp32 (|sum| <= 16 K = 2^19), so the oracle's bits are the bar."""
+    M, N, K = 256, 520, 32768
+    configure(g, plan, unit)
+    try:
+        A, B = draw(M, N, K, dist="int", seed=101)
+        C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), wl.F32))
+        C_ref, _ = oracle_full(A, B)
+        assert np.array_equal(C, C_ref), f"{int((C != C_ref).sum())} mismatches"
+    finally:
+        configure(g, plan, 4)
+
+
 def test_k_zero_writes_zeros(g, plan):
     for out in OUTS:
         A = torch.empty((37, 0), dtype=torch.bfloat16, device="cuda")
