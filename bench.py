@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -105,13 +106,21 @@ def load_peaks():
 DEVICE_SOURCES = ("gemm_kernel.cuh", "kernel_table.h", "kernels_inst.cu", "ptx.cuh", "schedule.h")
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments, trailing spaces and blank lines: a
+    comment edit does not change the kernel the counters were taken on."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300", "csrc")
     for name in DEVICE_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -60,21 +60,25 @@
 namespace gb300 {
 
 // Optional timeline tracing (build with -DGEMM_TRACE): per-CTA
-// %globaltimer stamps and wait totals in a device buffer of kTraceSlots
-// 64-bit words per CTA.  Without GEMM_TRACE the macros compile to nothing.
+// %globaltimer stamps, wait totals and SM cycle counts in a device buffer of
+// kTraceSlots 64-bit words per CTA.  Without GEMM_TRACE the macros compile
+// to nothing.  Slots 1, 2 and 10 are unused (their points are now cycle
+// stamps of the prologue, kTrClkPro).
 constexpr int kTraceSlots = 80;
 enum TraceSlot {
-    kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrFirstFull = 3, kTrTeardown = 4, kTrExit = 5,
-    kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8, kTrWorkItems = 9,
-    kTrFirstItem = 10,    // producer: first work item decoded
-    kTrEpiDone = 11,      // epilogue warp 2: all stores of the CTA complete
+    kTrEntry = 0,         // %globaltimer at entry (thread 0; written at teardown)
+    kTrFirstFull = 3,     // MMA warp: first full ring slot
+    kTrTeardown = 4, kTrExit = 5,
+    kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8,   // per-role wait totals
+    kTrWorkItems = 9,     // MMA warp: all work items issued
+    kTrEpiDone = 11,      // epilogue warp 2: the CTA's stores have read shared memory
     kTrClusterArrived = 12, kTrClusterDone = 13, kTrDealloc = 14,
-    kTrMmaEnd = 16,       // + item (8 items)
+    kTrClkFirstFull = 15, // SM cycles (clock64) at first_full ...
+    kTrMmaEnd = 16,       // + item (8 items): last MMA of the item issued
     kTrEpiStart = 24,     // + item
     kTrEpiEnd = 32,       // + item
     kTrPartialDone = 40,  // + item: stream-K partial published
-    kTrReduceDone = 48,   // + item: stream-K reduction finished (last contributor)
-    kTrClkFirstFull = 15, // SM clock cycles (clock64) at first_full ...
+    kTrReduceDone = 48,   // + item: stream-K tile finished (the piece holding its first k-blocks)
     kTrClkMmaEnd = 56,    // ... and at mma_end + item: cycles per k-block
     kTrClkPro = 64,       // + 0..8: SM cycles at the prologue steps (see timeline.PROLOGUE)
 };
