@@ -22,9 +22,9 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import re
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
