@@ -54,6 +54,7 @@ _lib.gemm_run.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run_host.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_run_layout.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp]
+_lib.gemm_plan_run_batched.argtypes = [_vp, _vp, _vp, _vp] + [_i64] * 7 + [_int, _int, _int, _vp]
 _lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp]
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
@@ -64,7 +65,7 @@ _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int)
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
-              "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
+              "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_run_batched", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
               "gemm_plan_last_launch",
               "gemm_plan_trace", "gemm_plan_destroy"):
     getattr(_lib, _name).restype = _int
@@ -119,6 +120,13 @@ def gemm_plan_run_layout(plan: int, A: int, B: int, C: int, M: int, N: int, K: i
                          out_dtype: int, layout: int, stream: int = 0) -> None:
     _check(_lib.gemm_plan_run_layout(_vp(plan), _vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, layout,
                                      _vp(stream)), "gemm_plan_run_layout")
+
+
+def gemm_plan_run_batched(plan: int, A: int, B: int, C: int, batch: int, M: int, N: int, K: int, stride_a: int,
+                          stride_b: int, stride_c: int, dtype: int, out_dtype: int, layout: int = 0,
+                          stream: int = 0) -> None:
+    _check(_lib.gemm_plan_run_batched(_vp(plan), _vp(A), _vp(B), _vp(C), batch, M, N, K, stride_a, stride_b,
+                                      stride_c, dtype, out_dtype, layout, _vp(stream)), "gemm_plan_run_batched")
 
 
 def gemm_plan_run_host(plan: int, A_host: int, B_host: int, C_host: int, M: int, N: int, K: int,
@@ -229,4 +237,30 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: boo
         gemm_run(*args)
     else:
         gemm_plan_run(plan, *args)
+    return out
+
+
+def bmm(A, B, plan: int, out_dtype=None, out=None):
+    """C[e] = A[e] @ B[e].T for CUDA tensors A [batch,M,K] or [M,K] (shared) and
+    B [batch,N,K] or [N,K] (shared), contiguous, same 16-bit or 8-bit dtype,
+    in one launch (gemm_plan_run_batched).  Returns C [batch,M,N]."""
+    import torch
+    if A.dim() not in (2, 3) or B.dim() not in (2, 3) or A.shape[-1] != B.shape[-1]:
+        raise ValueError("A must be [batch,M,K] or [M,K], B [batch,N,K] or [N,K]")
+    if A.dtype != B.dtype or not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous and of one dtype")
+    batch = A.shape[0] if A.dim() == 3 else B.shape[0] if B.dim() == 3 else 1
+    if (A.dim() == 3 and A.shape[0] != batch) or (B.dim() == 3 and B.shape[0] != batch):
+        raise ValueError("batch extents differ")
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-2]
+    if out_dtype is None:
+        out_dtype = A.dtype if A.element_size() == 2 else torch.bfloat16
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=out_dtype, device=A.device)
+    sa = M * K if A.dim() == 3 else 0
+    sb = N * K if B.dim() == 3 else 0
+    gemm_plan_run_batched(plan, A.data_ptr(), B.data_ptr(), out.data_ptr(), batch, M, N, K, sa, sb, M * N,
+                          _dtype_code(A.dtype), _dtype_code(out_dtype), 0,
+                          torch.cuda.current_stream(A.device).cuda_stream)
     return out

@@ -68,22 +68,33 @@ int get_encoder(EncodeTiledFn* out) {
     return GEMM_OK;
 }
 
-// Row-major matrix rows×cols (cols contiguous), box = box_rows × box_cols,
-// zero fill outside the matrix.
-int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+// A batch of row-major matrices rows×cols (cols contiguous), `count`
+// matrices `stride` elements apart, as a 3-D tensor map (cols, rows, batch);
+// box = box_rows × box_cols of one matrix; zero fill outside the tensor.  A
+// single matrix gets batch extent 1.
+int encode_3d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint64_t count,
+              uint64_t stride, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle,
+              CUtensorMapL2promotion promo) {
     EncodeTiledFn enc;
     int rc = get_encoder(&enc);
     if (rc != GEMM_OK) return rc;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes(dt)};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, tma_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const uint64_t eb = (uint64_t)elem_bytes(dt);
+    if (count <= 1) stride = rows * cols;
+    cuuint64_t dims[3] = {cols, rows, count < 1 ? 1 : count};
+    cuuint64_t strides[2] = {cols * eb, stride * eb};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, tma_dtype(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }
+
+// A batch of products: `count` problems with A, B, C `sa`, `sb`, `sc`
+// elements apart (0 for A or B: every problem uses the same matrix).
+struct Batch {
+    int64_t count = 1;
+    int64_t sa = 0, sb = 0, sc = 0;
+};
 
 // tcgen05 instruction descriptor: f32 accumulator, A and B K-major, M×N.
 // Operand format field (bits 7-9 for A, 10-12 for B): kind::f16 reads
@@ -201,10 +212,10 @@ bool width_fits_layout(int bn, int cluster, int layout) {
 }
 
 // Returns 0 when no width fits (a forced width the layout cannot use).
-int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int layout) {
+int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int layout, int64_t batch = 1) {
     if (plan->tile_n > 0) return width_fits_layout(plan->tile_n, cluster, layout) ? plan->tile_n : 0;
     const int64_t units = resident_units(plan, cluster);
-    const int64_t tiles_m = (M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster);
+    const int64_t tiles_m = batch * ((M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster));
     int best = 0;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < kNumTileWidths; ++i) {
@@ -221,16 +232,18 @@ int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int 
 }
 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
-           int out_dtype, cudaStream_t stream, int layout = 0) {
+           int out_dtype, cudaStream_t stream, int layout = 0, const Batch& batch = Batch()) {
     if (K == 0) {
         const size_t n16 = (size_t)M * (size_t)N * elem_bytes(out_dtype) / 16;
         const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)plan->sm_count * 8);
-        fill_zero_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(reinterpret_cast<uint4*>(C), n16);
+        for (int64_t e = 0; e < batch.count; ++e)
+            fill_zero_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(
+                reinterpret_cast<uint4*>(static_cast<char*>(C) + (size_t)(e * batch.sc) * elem_bytes(out_dtype)), n16);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
     const int cluster = unit_ctas(plan, K, dtype, layout);
-    const int bn = choose_tile_n(plan, M, N, cluster, layout);
+    const int bn = choose_tile_n(plan, M, N, cluster, layout, batch.count);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
     const bool pad = (layout & GEMM_B_MN_MAJOR) && !b_boxes_exact(bn, cluster);
     const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0, pad);
@@ -244,7 +257,11 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.tiles_n = (int)((N + bn - 1) / bn);
     const int64_t kbe = kblock_elems(dtype);
     p.k_blocks = (int)((K + kbe - 1) / kbe);
-    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.tiles_per_batch = p.tiles_m * p.tiles_n;
+    if ((int64_t)p.tiles_per_batch * batch.count >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    p.num_tiles = (int)(p.tiles_per_batch * batch.count);
+    p.a_batched = batch.count > 1 && batch.sa != 0;
+    p.b_batched = batch.count > 1 && batch.sb != 0;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
     p.idesc = make_idesc(dtype, kRowsPerCta * pair, bn, layout);   // one MMA covers a pair's 256 rows
@@ -266,21 +283,23 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     // K-major operand: rows of K, box {one 128-byte row of K, rows}.  MN-major
     // (A stored K×M, B stored K×N): rows of M or N, box {64 elements, the
     // k-block's K rows}, several boxes per stage.
+    const uint64_t na = p.a_batched ? (uint64_t)batch.count : 1, nb = p.b_batched ? (uint64_t)batch.count : 1;
     int rc = (layout & GEMM_A_MN_MAJOR)
-                 ? encode_2d(&tmA, dtype, A, (uint64_t)K, (uint64_t)M, (uint32_t)kbe, kMnBoxElems,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
-                 : encode_2d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, kRowsPerCta, (uint32_t)kbe,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                 ? encode_3d(&tmA, dtype, A, (uint64_t)K, (uint64_t)M, na, (uint64_t)batch.sa, (uint32_t)kbe,
+                             kMnBoxElems, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                 : encode_3d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, na, (uint64_t)batch.sa, kRowsPerCta,
+                             (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (rc == GEMM_OK)
         rc = (layout & GEMM_B_MN_MAJOR)
-                 ? encode_2d(&tmB, dtype, B, (uint64_t)K, (uint64_t)N, (uint32_t)kbe, kMnBoxElems,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
-                 : encode_2d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, (uint32_t)(bn / cluster), (uint32_t)kbe,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                 ? encode_3d(&tmB, dtype, B, (uint64_t)K, (uint64_t)N, nb, (uint64_t)batch.sb, (uint32_t)kbe,
+                             kMnBoxElems, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                 : encode_3d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, nb, (uint64_t)batch.sb,
+                             (uint32_t)(bn / cluster), (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
-        rc = encode_2d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, 32, kChunkCols,
-                       out_dtype == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+        rc = encode_3d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, (uint64_t)batch.count, (uint64_t)batch.sc, 32,
+                       kChunkCols, out_dtype == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc != GEMM_OK) return rc;
 
@@ -488,6 +507,28 @@ int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C
     int rc = validate(A, B, C, M, N, K, dtype, out_dtype, layout);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream), layout);
+}
+
+int gemm_plan_run_batched(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t batch, int64_t M,
+                          int64_t N, int64_t K, int64_t stride_a, int64_t stride_b, int64_t stride_c, int dtype,
+                          int out_dtype, int layout, void* stream) {
+    if (!plan || batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0) return GEMM_ERR_INVALID_ARG;
+    int rc = validate(A, B, C, M, N, K, dtype, out_dtype, layout);
+    if (rc != GEMM_OK || M == 0 || N == 0 || batch == 0) return rc;
+    if (batch > 1) {
+        // batch strides: 16-byte multiples (TMA), and no element shared by two outputs
+        const int64_t ib = elem_bytes(dtype), ob = elem_bytes(out_dtype);
+        if ((stride_a * ib) % 16 != 0 || (stride_b * ib) % 16 != 0 || (stride_c * ob) % 16 != 0)
+            return GEMM_ERR_UNSUPPORTED;
+        if (stride_c < M * N || (stride_a != 0 && stride_a < M * K) || (stride_b != 0 && stride_b < N * K))
+            return GEMM_ERR_INVALID_ARG;
+    }
+    Batch bt;
+    bt.count = batch;
+    bt.sa = stride_a;
+    bt.sb = stride_b;
+    bt.sc = stride_c;
+    return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream), layout, bt);
 }
 
 int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype, int out_dtype,

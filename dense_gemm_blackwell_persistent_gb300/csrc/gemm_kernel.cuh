@@ -136,6 +136,8 @@ struct Params {
     // constant-cache line.
     Schedule sched;    // whole-tile waves + stream-K part
     int tiles_m, tiles_n, group_m, k_blocks;
+    int tiles_per_batch;        // tiles_m * tiles_n; tile t is in batch element t / tiles_per_batch
+    int a_batched, b_batched;   // 0: every batch element reads the same A / B (batch coordinate 0)
     int M, N, K, num_tiles;
     uint32_t idesc;
     int* status;       // [0] first error code, [1] role, [2] block, [3] detail
@@ -231,10 +233,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Output tile of linear tile index t: groups of `group_m` tile rows are
-// walked column by column, so the tiles in flight at once share rows of A
-// and columns of Bᵀ in L2.
-__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mt, int& nt) {
+// Output tile of linear tile index t: batch element bt = t / tiles_per_batch;
+// within it, groups of `group_m` tile rows are walked column by column, so
+// the tiles in flight at once share rows of A and columns of Bᵀ in L2.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& bt, int& mt, int& nt) {
+    bt = t / p.tiles_per_batch;
+    t -= bt * p.tiles_per_batch;
     const int per_group = p.group_m * p.tiles_n;
     const int g = t / per_group;
     const int first_m = g * p.group_m;
@@ -366,9 +370,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     // Operand rows of this CTA for output tile `tile` (A: its 128 rows; B: the
     // rows of the pair's B tile that this CTA loads).
-    auto operand_rows = [&](int tile, int& a_row, int& b_row) {
+    auto operand_rows = [&](int tile, int& a_row, int& b_row, int& bt) {
         int mt, nt;
-        tile_coords(p, tile, mt, nt);
+        tile_coords(p, tile, bt, mt, nt);
         a_row = mt * C::kTileM + (int)crank * kRowsPerCta;
         b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
     };
@@ -432,8 +436,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int nwork = work_count(p.sched, pair_id);
             for (int j = 0; j < nwork && ok; ++j) {
                 const Work w = work_item(p.sched, pair_id, j);
-                int a_row, b_row;
-                operand_rows(w.tile, a_row, b_row);
+                int a_row, b_row, bt;
+                operand_rows(w.tile, a_row, b_row, bt);
+                const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;   // batch coordinates
                 if (j == 0 && lane == 0) GEMM_TR_CLK(5);
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     const uint64_t tw = GEMM_TR_NOW();
@@ -456,13 +461,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         const uint32_t fb_leader = kCluster > 1 ? map_shared_rank(fb, leader) : fb;
                         const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
                         auto copy_a = [&](uint32_t dst, int x, int y) {
-                            if constexpr (kCluster > 1) tma_load_2d_pair(dst, &tmA, fb_leader, x, y);
-                            else tma_load_2d(dst, &tmA, fb, x, y);
+                            if constexpr (kCluster > 1) tma_load_3d_pair(dst, &tmA, fb_leader, x, y, za);
+                            else tma_load_3d(dst, &tmA, fb, x, y, za);
                         };
                         auto copy_b = [&](uint32_t dst, int x, int y) {
-                            if constexpr (kCluster == 4) tma_load_2d_pair_multicast(dst, &tmB, fb_leader, mask, x, y);
-                            else if constexpr (kCluster == 2) tma_load_2d_pair(dst, &tmB, fb_leader, x, y);
-                            else tma_load_2d(dst, &tmB, fb, x, y);
+                            if constexpr (kCluster == 4)
+                                tma_load_3d_pair_multicast(dst, &tmB, fb_leader, mask, x, y, zb);
+                            else if constexpr (kCluster == 2) tma_load_3d_pair(dst, &tmB, fb_leader, x, y, zb);
+                            else tma_load_3d(dst, &tmB, fb, x, y, zb);
                         };
                         const int kx = kb * C::kBlockKElems;
                         const uint32_t b_q = b_dst + pidx * C::kLoadBytesB;
@@ -610,8 +616,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         };
         // Stage one chunk in this warp's two staging boxes and TMA-store it to
-        // C at (ccol, row0).
-        auto store_chunk = [&](const uint32_t (&cur)[32], int ccol, int row0) {
+        // C at (ccol, row0) of batch element bt.
+        auto store_chunk = [&](const uint32_t (&cur)[32], int ccol, int row0, int bt) {
             const uint32_t buf = staging + (slot & 1u) * C::kSlotBytes;
             ++slot;
             if (lane == 0) bulk_wait_group_read<1>();   // the store that last read `buf` is done
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(&tmC, buf, ccol, row0);
+                tma_store_3d(&tmC, buf, ccol, row0, bt);
                 bulk_commit_group();
             }
         };
@@ -633,8 +639,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!__all_sync(0xffffffffu, got)) break;
             if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiStart, i);
             tc_fence_after_sync();
-            int mt, nt;
-            tile_coords(p, w.tile, mt, nt);
+            int bt, mt, nt;
+            tile_coords(p, w.tile, bt, mt, nt);
             const int row0 = mt * C::kTileM + (int)crank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         for (int c = 0; c < kChunks && col0 + c * kChunkCols < p.N; ++c)
-                            tma_store_2d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0);
+                            tma_store_3d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0, bt);
                         bulk_commit_group();
                     }
                 }
@@ -677,7 +683,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
                         if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
                         const int ccol = col0 + c * kChunkCols;
-                        if (ccol < p.N) store_chunk(cur, ccol, row0);
+                        if (ccol < p.N) store_chunk(cur, ccol, row0, bt);
                         if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
                 }
@@ -742,7 +748,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 for (int e = 0; e < 4; ++e)
                                     sum[4 * q + e] = __float_as_uint(__uint_as_float(cur[4 * q + e]) + __uint_as_float(o[e]));
                             }
-                            store_chunk(sum, ccol, row0);
+                            store_chunk(sum, ccol, row0, bt);
                         }
                         if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }

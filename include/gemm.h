@@ -153,6 +153,20 @@ int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64
 int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t M, int64_t N,
                          int64_t K, int dtype, int out_dtype, int layout, void* stream);
 
+/* A batch of products C_e = A_e·B_eᵀ, e < batch, in one persistent launch
+ * over batch × tiles output tiles: A_e at A + e·stride_a, B_e at
+ * B + e·stride_b, C_e at C + e·stride_c (strides in elements).  stride_a or
+ * stride_b 0: every product reads the same A or B — the batched matmul with
+ * a shared operand of "Chapter 7: Writing Custom Kernels with Pallas", §5.2
+ * (vmap with in_axes=(0, None)).  Shapes, `layout` flags and their rules
+ * as gemm_plan_run_layout, for every element.  With batch > 1: each stride
+ * times its element size a multiple of 16 bytes (GEMM_ERR_UNSUPPORTED), and
+ * no overlap: stride_c >= M·N, stride_a 0 or >= M·K, stride_b 0 or >= N·K
+ * (GEMM_ERR_INVALID_ARG).  batch 0 is a no-op. */
+int gemm_plan_run_batched(gemm_plan_t plan, const void* A, const void* B, void* C, int64_t batch, int64_t M,
+                          int64_t N, int64_t K, int64_t stride_a, int64_t stride_b, int64_t stride_c, int dtype,
+                          int out_dtype, int layout, void* stream);
+
 /* End-to-end form for callers whose operands live in host memory: copies A
  * and B (host, ideally pinned) to device buffers the plan owns (grown on
  * demand and kept for reuse), runs the product, copies C back to host

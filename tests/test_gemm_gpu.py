@@ -427,6 +427,108 @@ def test_operand_major_b_every_tile_width(g, fresh_plan, unit, tile_n, layout):
     assert np.array_equal(C, C_ref), f"{int((C != C_ref).sum())} mismatches"
 
 
+# ------------------------------------------------------------------ batched products
+
+# (batch, M, N, K, A shared, B shared, layout, stride padding in elements)
+BATCH_CASES = [
+    # the shape of the batched masked matmul of "Chapter 7: Writing Custom
+    # Kernels with Pallas", §5.2 (vmap over 3, B K×N shared), with N 130 -> 136
+    # so that rows are 16-byte multiples
+    (3, 100, 136, 200, False, True, 2, 0),
+    (4, 260, 520, 264, False, False, 0, 64),    # separate A and B, padded batch strides
+    (5, 256, 264, 136, True, False, 0, 0),      # A shared
+    (2, 1000, 776, 392, False, False, 3, 8),    # both operands MN-major
+]
+
+
+def run_batched(g, plan, As, Bs, case, out):
+    """As: [batch,M,K] CPU tensors (or one shared [M,K]); Bs likewise [N,K]."""
+    batch, M, N, K, a_sh, b_sh, layout, pad = case
+    dt = CODE_OF[As.dtype]
+
+    def stage(X, rows, cols, shared, mn):
+        # device storage: each element row-major (or its transpose for an MN-major operand), `pad` apart
+        mats = [X] if shared else [X[e] for e in range(batch)]
+        mats = [m.t().contiguous() if mn else m.contiguous() for m in mats]
+        if shared:
+            return mats[0].cuda(), 0
+        stride = rows * cols + pad
+        buf = torch.zeros(batch * stride, dtype=X.dtype)
+        for e, m in enumerate(mats):
+            buf[e * stride:e * stride + rows * cols] = m.reshape(-1)
+        return buf.cuda(), stride
+
+    Ad, sa = stage(As, M, K, a_sh, layout & 1)
+    Bd, sb = stage(Bs, N, K, b_sh, layout & 2)
+    sc = M * N + pad
+    C = torch.full((batch * sc,), float("nan"), dtype=TORCH[out], device="cuda")
+    g.gemm_plan_run_batched(plan, Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), batch, M, N, K, sa, sb, sc, dt, out,
+                            layout, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+    C = C.cpu()
+    if pad:
+        assert bool(torch.isnan(C.view(batch, sc)[:, M * N:].float()).all()), "padding between outputs was written"
+    return [C[e * sc:e * sc + M * N].view(M, N) for e in range(batch)]
+
+
+def draw_batch(case, dist, dtype=wl.BF16, seed=0):
+    batch, M, N, K, a_sh, b_sh, _, _ = case
+    A, B = draw(M * (1 if a_sh else batch), N * (1 if b_sh else batch), K, dtype=dtype, dist=dist, seed=seed)
+    As = A if a_sh else A.view(batch, M, K)
+    Bs = B if b_sh else B.view(batch, N, K)
+    return As, Bs
+
+
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("case", BATCH_CASES, ids=lambda c: "b{}x{}x{}x{}".format(*c[:4]))
+def test_batched_integer_bit_exact(g, plan, unit, case):
+    batch, M, N, K, a_sh, b_sh, layout, pad = case
+    configure(g, plan, unit)
+    try:
+        As, Bs = draw_batch(case, "int", seed=batch * 10 + unit)
+        Cs = run_batched(g, plan, As, Bs, case, wl.F32)
+        for e in range(batch):
+            Ae = As if a_sh else As[e]
+            Be = Bs if b_sh else Bs[e]
+            C_ref, _ = oracle_full(Ae.contiguous(), Be.contiguous())
+            assert np.array_equal(parity.to_f64(Cs[e]), C_ref), f"batch element {e}"
+    finally:
+        configure(g, plan, 4)
+
+
+def test_batched_random_within_tolerance(g, plan):
+    case = (3, 520, 776, 1008, False, False, 0, 0)   # K % 16 == 0 for the 8-bit case
+    for dtype, out in ((wl.BF16, wl.BF16), (wl.F16, wl.F16), (wl.E4M3, wl.F32)):
+        As, Bs = draw_batch(case, "normal", dtype=dtype, seed=7)
+        Cs = run_batched(g, plan, As, Bs, case, out)
+        for e in range(case[0]):
+            C_ref, S = oracle_full(As[e].contiguous(), Bs[e].contiguous())
+            parity.assert_within(parity.to_f64(Cs[e]), C_ref, S, out, f"batch {e} dtype {dtype}")
+
+
+def test_bmm_helper_and_rules(g, plan):
+    import ctypes
+    A, B = draw(3 * 264, 200, 136, seed=5)
+    A3 = A.view(3, 264, 136).cuda()
+    C = g.bmm(A3, B.cuda(), plan, out_dtype=torch.float32)      # B shared
+    torch.cuda.synchronize()
+    for e in range(3):
+        C_ref, S = oracle_full(A[e * 264:(e + 1) * 264], B)
+        parity.assert_within(parity.to_f64(C[e]), C_ref, S, wl.F32, f"bmm {e}")
+    vp = ctypes.c_void_p
+    X = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros(4096, dtype=torch.float32, device="cuda")
+    args = (vp(plan), vp(X.data_ptr()), vp(X.data_ptr()), vp(Y.data_ptr()))
+    rs = g.raw_status
+    assert rs("gemm_plan_run_batched", *args, 2, 16, 16, 16, 256, 256, 200, 0, 2, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_run_batched", *args, 2, 16, 16, 16, 260, 256, 256, 0, 2, 0, None) == g.GEMM_ERR_UNSUPPORTED
+    assert rs("gemm_plan_run_batched", *args, -1, 16, 16, 16, 256, 256, 256, 0, 2, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert rs("gemm_plan_run_batched", *args, 0, 16, 16, 16, 256, 256, 256, 0, 2, 0, None) == g.GEMM_OK
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm_4096_bf16", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16",
