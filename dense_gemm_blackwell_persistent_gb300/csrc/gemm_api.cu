@@ -194,11 +194,6 @@ int resident_units(const gemm_plan* plan, int cluster) {
     return std::max(1, units);
 }
 
-// Tile width: the candidate that minimises (waves of resident units) ×
-// (BN + 48).  The per-K-block time of the kernel measured on GB300 grows as
-// BN + 48 (316 / 242 / 183 ns for BN = 256 / 192 / 128 with CTA pairs at
-// 8192³), so a narrower tile pays off when it fills the last wave: 224 at
-// 4096³ (4 full waves instead of 3.4) and at 1024×4096×4096.
 // With an MN-major B, whether every CTA's share of the tile's B rows (as
 // held for the MMA and as loaded) is whole 64-element TMA boxes.  If not, a
 // 1- or 2-CTA unit uses the padded kernel form (shares rounded up to whole
@@ -211,19 +206,31 @@ bool width_fits_layout(int bn, int cluster, int layout) {
     return !(layout & GEMM_B_MN_MAJOR) || cluster <= 2 || b_boxes_exact(bn, cluster);
 }
 
-// Returns 0 when no width fits (a forced width the layout cannot use).
+// Tile width: the candidate that minimises (waves of resident units) × (SM
+// cycles per k-block of that width), preferring the wider tile when two are
+// within 1%.  Cycles per k-block measured on GB300 at 8192³ (GEMM_TRACE
+// cycle stamps, steady state): CTA pairs (also the 4-CTA multicast unit)
+// 520 / 453 / 432 / 429 / 485 for widths 256 / 224 / 192 / 160 / 128 —
+// only 256 and 224 run at the MMA's own rate, narrower tiles hit a floor —
+// and single CTAs 673 / 652 / 528 / 506 / 482.  So 224 is picked at 4096³
+// (304 tiles = 4 whole waves on 76 pairs) and at 1024×4096×4096, 256 at
+// 8192³.  Returns 0 when no width fits (a forced width the layout cannot
+// use).
 int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int layout, int64_t batch = 1) {
     if (plan->tile_n > 0) return width_fits_layout(plan->tile_n, cluster, layout) ? plan->tile_n : 0;
+    static constexpr int64_t kCyclesPair[kNumTileWidths] = {520, 453, 432, 429, 485};
+    static constexpr int64_t kCyclesSingle[kNumTileWidths] = {673, 652, 528, 506, 482};
+    const int64_t* cycles = cluster >= 2 ? kCyclesPair : kCyclesSingle;
     const int64_t units = resident_units(plan, cluster);
     const int64_t tiles_m = batch * ((M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster));
     int best = 0;
     int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < kNumTileWidths; ++i) {
+    for (int i = 0; i < kNumTileWidths; ++i) {   // widest first
         const int bn = kTileWidths[i];
         if (!width_fits_layout(bn, cluster, layout)) continue;
         const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
-        const int64_t cost = ((tiles + units - 1) / units) * (bn + 48);
-        if (cost < best_cost) {   // ties keep the wider tile
+        const int64_t cost = ((tiles + units - 1) / units) * cycles[i];
+        if (cost * 100 < best_cost * 99) {   // a narrower tile must be > 1% cheaper
             best_cost = cost;
             best = bn;
         }
