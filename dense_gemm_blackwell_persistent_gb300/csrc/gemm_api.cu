@@ -127,6 +127,7 @@ struct gemm_plan {
     int cap_ctas = 0;
     int tile_n = 0;               // 0 = 256
     int stream_k = 0;             // split the K work of a partial last wave (option)
+    int dynamic = -1;             // run-time tile hand-out: 0 off, 1 the partial last wave, 2 every tile, -1 auto
     int64_t wait_limit_us = 0;    // bound on a kernel wait (0 = kWaitLimitNs)
     int stall_test = 0;           // tests of the timeout path only
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
@@ -172,6 +173,13 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     if (((layout & GEMM_B_MN_MAJOR) ? N * ib : K * ib) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     if ((N * elem_bytes(out_dtype)) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
     return GEMM_OK;
+}
+
+// CTAs the device keeps resident with the largest unit size that fits
+// best; the plan's per-CTA buffers (stream-K workspace, trace) are sized
+// for this many.
+int max_resident_ctas(const gemm_plan* plan) {
+    return std::max(plan->max_ctas[1], std::max(plan->max_ctas[2], plan->max_ctas[4]));
 }
 
 // CTAs per work unit: 1 (single CTA), 2 (a CTA pair) or 4 (two pairs
@@ -238,6 +246,44 @@ int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int 
     return best;
 }
 
+// Dynamic work list of a launch (cluster launch control): `units`
+// persistent clusters with `waves` whole tiles each, then one single-tile
+// cluster per remaining tile.  Mode 1 hands out only the partial last
+// wave (the whole waves keep the static placement of tiles on SMs); mode 2
+// every tile.  Returns false for the static schedule: mode 0, or mode 1
+// when the tiles fill whole waves or fit in one.
+//
+// Automatic choice: mode 1 from kDynamicMinWaves whole waves on.  On GB300
+// some SMs run a 256-wide tile up to 4% slower than others (the same SMs in
+// every launch), so over many waves the static units drift apart and the
+// slowest one sets the end; handing out the partial last wave lets the
+// fast units take it.  Measured against the static schedule: 8192³ 588 →
+// 570 µs, 7168³ 389 → 384, 8192×8192×4096 291 → 286, 8192×4096×8192 294 →
+// 289, 5120³ 158 → 155 (6 to 13 waves); level at 3 to 5 waves; slower by
+// 1.5-4 µs at 1 or 2 waves (3072³, 3328×4096×4096, 4000×3000×5000), where
+// the drift is small and the handed-out tiles lose the static placement
+// (~5% slower per tile when every tile is handed out).  Mode 2 measured
+// slower than mode 1 almost everywhere.  Plans with a CTA cap or stream-K
+// keep the static schedule unless mode 1 or 2 is set explicitly.
+constexpr int64_t kDynamicMinWaves = 6;
+
+bool dynamic_lists(const gemm_plan* plan, int64_t tiles, int64_t resident, int* units, int* waves) {
+    int mode = plan->dynamic;
+    if (mode < 0)
+        mode = (plan->cap_ctas == 0 && !plan->stream_k && tiles / resident >= kDynamicMinWaves) ? 1 : 0;
+    if (mode == 2) {
+        *units = (int)tiles;
+        *waves = 1;
+        return true;
+    }
+    if (mode == 1 && tiles > resident && tiles % resident != 0) {
+        *units = (int)resident;
+        *waves = (int)(tiles / resident);
+        return true;
+    }
+    return false;
+}
+
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
            int out_dtype, cudaStream_t stream, int layout = 0, const Batch& batch = Batch()) {
     if (K == 0) {
@@ -276,15 +322,23 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.b_mn = (layout & GEMM_B_MN_MAJOR) ? 1 : 0;
     p.status = plan->d_status;
     // Stream-K spreads a partial last wave over every resident unit; with
-    // whole tiles only, never launch more units than tiles.
+    // whole tiles only, never launch more units than tiles.  A dynamic work
+    // list launches one cluster per list (clusters that do not start are
+    // cancelled by running ones, which do their lists).
     const int resident = resident_units(plan, cluster);
-    const bool sk = plan->stream_k && plan->d_partials != nullptr && plan->d_flags != nullptr;
+    int dyn_units = 0, dyn_waves = 0;
+    const bool dyn = dynamic_lists(plan, p.num_tiles, resident, &dyn_units, &dyn_waves);
+    const bool sk = !dyn && plan->stream_k && plan->d_partials != nullptr && plan->d_flags != nullptr;
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
+    p.dynamic = dyn ? 1 : 0;
+    p.dyn_units = dyn_units;
+    p.dyn_waves = dyn_waves;
     p.partials = plan->d_partials;
     p.flags = plan->d_flags;
     p.wait_limit_ns = plan->wait_limit_us > 0 ? (unsigned long long)plan->wait_limit_us * 1000ull : kWaitLimitNs;
     p.stall_test = plan->stall_test;
     p.trace = plan->d_trace;
+    p.trace_ctas = max_resident_ctas(plan);
 
     CUtensorMap tmA, tmB, tmC;
     // K-major operand: rows of K, box {one 128-byte row of K, rows}.  MN-major
@@ -310,7 +364,8 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc != GEMM_OK) return rc;
 
-    const int units = p.sched.units;
+    // clusters launched: the static schedule's units, or one per dynamic list
+    const int units = dyn ? dyn_units + (p.num_tiles - dyn_units * dyn_waves) : p.sched.units;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * cluster), 1, 1);
@@ -332,16 +387,9 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     plan->last_grid = units * cluster;
     plan->last_tile_n = bn;
     plan->last_unit = cluster;
-    plan->last_dp_waves = p.sched.dp_waves;
+    plan->last_dp_waves = dyn ? (dyn_units == p.num_tiles ? 0 : dyn_waves) : p.sched.dp_waves;
     plan->last_sk_tiles = p.sched.sk_tiles;
     return GEMM_OK;
-}
-
-// Stream-K workspace: two partial slots per unit; a slot holds kPair CTAs ×
-// 4 epilogue warps × 32×256 fp32, i.e. 128 KB per CTA, for every CTA the
-// device can keep resident.
-int max_resident_ctas(const gemm_plan* plan) {
-    return std::max(plan->max_ctas[1], std::max(plan->max_ctas[2], plan->max_ctas[4]));
 }
 
 // One partial slot per unit: 4 epilogue warps × 32 rows × 256 fp32 per CTA.
@@ -483,6 +531,10 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
         case GEMM_OPT_STALL_TEST:
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             plan->stall_test = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_DYNAMIC:
+            if (value < -1 || value > 2) return GEMM_ERR_INVALID_ARG;
+            plan->dynamic = (int)value;
             return GEMM_OK;
         case GEMM_OPT_TILE_N: {
             if (value == 0) {

@@ -62,15 +62,16 @@ namespace gb300 {
 // Optional timeline tracing (build with -DGEMM_TRACE): per-CTA
 // %globaltimer stamps, wait totals and SM cycle counts in a device buffer of
 // kTraceSlots 64-bit words per CTA.  Without GEMM_TRACE the macros compile
-// to nothing.  Slots 1, 2 and 10 are unused (their points are now cycle
-// stamps of the prologue, kTrClkPro).
+// to nothing.
 constexpr int kTraceSlots = 80;
 enum TraceSlot {
     kTrEntry = 0,         // %globaltimer at entry (thread 0; written at teardown)
+    kTrClcWaitProducerNs = 1, kTrClcWaitEpiNs = 2,   // dynamic work list: time waiting for responses
     kTrFirstFull = 3,     // MMA warp: first full ring slot
     kTrTeardown = 4, kTrExit = 5,
     kTrFullWaitNs = 6, kTrEmptyWaitNs = 7, kTrAccEmptyWaitNs = 8,   // per-role wait totals
     kTrWorkItems = 9,     // MMA warp: all work items issued
+    kTrClcWaitMmaNs = 10,
     kTrEpiDone = 11,      // epilogue warp 2: the CTA's stores have read shared memory
     kTrClusterArrived = 12, kTrClusterDone = 13, kTrDealloc = 14,
     kTrClkFirstFull = 15, // SM cycles (clock64) at first_full ...
@@ -81,11 +82,13 @@ enum TraceSlot {
     kTrReduceDone = 48,   // + item: stream-K tile finished (the piece holding its first k-blocks)
     kTrClkMmaEnd = 56,    // ... and at mma_end + item: cycles per k-block
     kTrClkPro = 64,       // + 0..8: SM cycles at the prologue steps (see timeline.PROLOGUE)
+    kTrDynTile = 72,      // + 1 + r (r < 7): the list (cluster) that response r handed to this unit
 };
 #ifdef GEMM_TRACE
-#define GEMM_TR(slot) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
+#define GEMM_TR_ON() (p.trace && blockIdx.x < (unsigned)p.trace_ctas)
+#define GEMM_TR(slot) do { if (GEMM_TR_ON()) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
 #define GEMM_TR_ITEM(base, item) do { if ((item) < 8) GEMM_TR((base) + (item)); } while (0)
-#define GEMM_TR_SET(slot, v) do { if (p.trace) p.trace[blockIdx.x * kTraceSlots + (slot)] = (v); } while (0)
+#define GEMM_TR_SET(slot, v) do { if (GEMM_TR_ON()) p.trace[blockIdx.x * kTraceSlots + (slot)] = (v); } while (0)
 #define GEMM_TR_NOW() global_timer_ns()
 // Prologue cycle stamps stay in registers (constant indices) until the
 // teardown writes them, so that taking them costs a few cycles and no
@@ -94,10 +97,10 @@ enum TraceSlot {
 #define GEMM_TR_CLK(step) (tr_clk[(step)] = (unsigned long long)clock64())
 #define GEMM_TR_CLK_FLUSH()                                                            \
     do {                                                                               \
-        if (p.trace)                                                                   \
+        if (GEMM_TR_ON())                                                              \
             for (int s_ = 0; s_ < 9; ++s_)                                             \
                 if (tr_clk[s_]) p.trace[blockIdx.x * kTraceSlots + kTrClkPro + s_] = tr_clk[s_]; \
-        if (p.trace && tr_entry_ns) p.trace[blockIdx.x * kTraceSlots + kTrEntry] = tr_entry_ns;      \
+        if (GEMM_TR_ON() && tr_entry_ns) p.trace[blockIdx.x * kTraceSlots + kTrEntry] = tr_entry_ns; \
     } while (0)
 #else
 #define GEMM_TR_CLK_FLUSH() do { } while (0)
@@ -121,6 +124,11 @@ constexpr int kAccStride = 256;          // TMEM columns between the two accumul
 constexpr int kTmemCols = 2 * kAccStride;
 constexpr int kStageBytesA = kRowsPerCta * kBlockKBytes;
 constexpr int kChunkCols = 32;           // accumulator columns per epilogue store box
+// Dynamic scheduling: responses of cluster launch control in flight or not
+// yet read by every role of the cluster (a ring, so that the issuer never
+// overwrites a response a lagging epilogue warp has still to read).
+constexpr int kClcSlots = 4;
+constexpr uint32_t kClcResponseBytes = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default bound on any single wait
 constexpr int kRoleStallTest = 8;  // status[1] of the timeout a test provokes on purpose
 
@@ -130,11 +138,16 @@ constexpr int kErrCuda = -4;      // device side: the launch's shared memory is 
 constexpr int kErrTimeout = -7;
 constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the base address
 constexpr int kRoleLayout = 10;   // status[1] for kErrCuda: an MN-major operand this tile cannot hold
+constexpr int kRoleClc = 11;      // status[1] of a timeout on the dynamic work list's ring (detail: item)
 
 struct Params {
     // What decoding a work item reads comes first, so that it shares one
     // constant-cache line.
     Schedule sched;    // whole-tile waves + stream-K part
+    // Dynamic work list (cluster launch control): 1 = on.  Cluster c < dyn_units
+    // owns tiles c, c + dyn_units, ... (dyn_waves of them); cluster c >=
+    // dyn_units owns tile dyn_units * dyn_waves + (c - dyn_units).
+    int dynamic, dyn_units, dyn_waves;
     int tiles_m, tiles_n, group_m, k_blocks;
     int tiles_per_batch;        // tiles_m * tiles_n; tile t is in batch element t / tiles_per_batch
     int a_batched, b_batched;   // 0: every batch element reads the same A / B (batch coordinate 0)
@@ -147,6 +160,7 @@ struct Params {
     int stall_test;    // 1: the MMA warp waits on a barrier nothing completes (tests of the timeout path)
     int a_mn, b_mn;    // 1: A stored K×M / B stored K×N (MN-major in shared memory)
     unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
+    int trace_ctas;             // CTAs the trace buffer holds (CTAs with a higher index record nothing)
 };
 
 // fp32 partial of one epilogue warp: 32 rows × 256 columns, stored as
@@ -186,7 +200,8 @@ struct Cfg {
     static constexpr int kSlotBytes = 32 * kRowBytes;           // one 32-row store box
     static constexpr int kStagingBytes = kEpiWarps * 2 * kSlotBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kFixed = kStagingBytes + kBarBytes + 16;
+    static constexpr int kMiscBytes = 16 + kClcSlots * (int)kClcResponseBytes;   // TMEM address, abort flag; responses
+    static constexpr int kFixed = kStagingBytes + kBarBytes + kMiscBytes;
     static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static_assert(kStages >= 3, "ring too shallow");
@@ -194,9 +209,11 @@ struct Cfg {
     static constexpr int kOffStaging = kOffB + kStages * kStageBytesB;
     static constexpr int kOffBars = kOffStaging + kStagingBytes;
     static constexpr int kOffMisc = kOffBars + kBarBytes;
-    static constexpr int kSmemBytes = kOffMisc + 16;
+    static constexpr int kOffClc = kOffMisc + 16;   // the responses (kOffMisc is 1 KB + kBarBytes aligned)
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert((2 * kStages + 4 + kEpiWarps) * 8 <= kBarBytes, "barrier area");
+    static_assert((2 * kStages + 4 + kEpiWarps + 2 * kClcSlots) * 8 <= kBarBytes, "barrier area");
+    static_assert(kOffClc % 16 == 0, "cluster launch control responses are 16-byte aligned");
     static constexpr uint32_t kPartialBytes = kBN * 32 * 4;   // one epilogue warp's fp32 partial
     static_assert(kEpiWarps * kFixupBytes <= kOffStaging, "fix-up buffers must fit in the operand ring");
     static_assert(kEpiWarps * (kBN / kChunkCols) * kSlotBytes <= kOffStaging,
@@ -358,6 +375,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto accf_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };
     auto fix_bar = [&](int e) { return bars + 8u * (2 * kStages + 4 + e); };   // per epilogue warp
+    auto clc_full = [&](int s) { return bars + 8u * (2 * kStages + 4 + kEpiWarps + s); };
+    auto clc_empty = [&](int s) { return bars + 8u * (2 * kStages + 4 + kEpiWarps + kClcSlots + s); };
+    auto clc_resp = [&](int s) { return base + (uint32_t)C::kOffClc + kClcResponseBytes * (uint32_t)s; };
+    // Readers of each response: every CTA's producer and epilogue warps and
+    // each pair's MMA warp.
+    constexpr int kClcReaders = kCluster * (1 + kEpiWarps) + C::kPairs;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
 
@@ -377,6 +400,63 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         b_row = nt * kBN + (int)rank * C::kRowsB + (int)pidx * C::kRowsBLoad;
     };
 
+    // ---- the work list
+    // Static: the schedule's items for this unit.  Dynamic ("Writing Mosaic
+    // GPU kernels with Pallas", "Cluster launch control"): the grid has one
+    // cluster per list of tiles -- the persistent units' lists of whole waves
+    // and one single-tile list per tile of the partial last wave (or one per
+    // tile of the problem).  A cluster does its own list, then the lists of
+    // clusters that have not started, which the hardware cancels on its
+    // request, until a request finds none left; so units that run fast
+    // take the tail.  The producer of the cluster's first CTA sends request r
+    // when it starts the last item of a list; the response lands in ring
+    // slot r % kClcSlots of every CTA of the cluster, and each reading warp
+    // releases the slot on the first CTA's empty barrier.  Nothing is
+    // requested after a request that failed.
+    const bool dyn = p.dynamic != 0;
+    const int nwork = dyn ? 0 : work_count(p.sched, pair_id);
+    auto list_len = [&](int c) { return c < p.dyn_units ? p.dyn_waves : 1; };
+    auto list_tile = [&](int c, int k) {
+        return c < p.dyn_units ? c + k * p.dyn_units : p.dyn_units * p.dyn_waves + (c - p.dyn_units);
+    };
+    // Position in this unit's work: whose list, the next item in it, its
+    // length, the next response to read.
+    struct Cursor {
+        int owner, pos, len, resp;
+    };
+    const Cursor cursor0 = {pair_id, 0, dyn ? list_len(pair_id) : nwork, 0};
+    uint64_t clc_wait_ns = 0;   // trace builds only
+    // The next item of cursor `cur` into w: 1 = there is one, 0 = the work
+    // has ended, -1 = a wait gave up.  Called by whole warps.
+    auto get_work = [&](Cursor& cur, Work& w) -> int {
+        if (!dyn) {
+            if (cur.pos >= cur.len) return 0;
+            w = work_item(p.sched, pair_id, cur.pos++);
+            return 1;
+        }
+        while (cur.pos >= cur.len) {
+            const int r = cur.resp++, s = r % kClcSlots;
+            const uint64_t tw = GEMM_TR_NOW();
+            if (!__all_sync(0xffffffffu, wait_bounded<(kCluster > 1)>(clc_full(s), (uint32_t)(r / kClcSlots) & 1u,
+                                                                       abort_flag, p, kRoleClc, r)))
+                return -1;
+            clc_wait_ns += GEMM_TR_NOW() - tw;
+            const int x = clc_response(clc_resp(s));
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (kCluster > 1) mbar_arrive_cluster(map_shared_rank(clc_empty(s), 0));
+                else mbar_arrive_local(clc_empty(s));
+            }
+            if (x < 0) return 0;
+            cur.owner = x / kCluster;
+            cur.pos = 0;
+            cur.len = list_len(cur.owner);
+            if (warp == 0 && lane == 0 && r < 7) GEMM_TR_SET(kTrDynTile + 1 + r, (unsigned long long)cur.owner + 1);
+        }
+        w = whole_tile(list_tile(cur.owner, cur.pos++), p.k_blocks);
+        return 1;
+    };
+
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -388,6 +468,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(acce_bar(b), kEpiWarps * kPair);
         }
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(fix_bar(e), 1);
+        for (int s = 0; s < kClcSlots; ++s) {
+            mbar_init(clc_full(s), 1);              // the requester's expect-tx arrival + 16 bytes
+            mbar_init(clc_empty(s), kClcReaders);   // used in the cluster's first CTA
+        }
         *abort_flag = 0;
         fence_mbar_init_cluster();
         GEMM_TR_CLK(1);
@@ -433,9 +517,38 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             uint64_t empty_wait_ns = 0;   // trace builds only
-            const int nwork = work_count(p.sched, pair_id);
-            for (int j = 0; j < nwork && ok; ++j) {
-                const Work w = work_item(p.sched, pair_id, j);
+            // Request r of the dynamic list: once every reader has released
+            // slot r % kClcSlots, announce its 16 bytes on each CTA's full
+            // barrier and send the request.
+            auto request = [&](int r) -> bool {
+                const int s = r % kClcSlots;
+                if (!__all_sync(0xffffffffu,
+                                wait_bounded<(kCluster > 1)>(clc_empty(s), ((uint32_t)(r / kClcSlots) & 1u) ^ 1u,
+                                                             abort_flag, p, kRoleClc, -1 - r)))
+                    return false;
+                if (issuer) {
+                    if constexpr (kCluster > 1) {
+                        for (uint32_t c = 0; c < (uint32_t)kCluster; ++c)
+                            mbar_arrive_expect_tx_cluster(map_shared_rank(clc_full(s), c), kClcResponseBytes);
+                    } else {
+                        mbar_arrive_expect_tx(clc_full(s), kClcResponseBytes);
+                    }
+                    clc_try_cancel<(kCluster > 1)>(clc_resp(s), clc_full(s));
+                }
+                __syncwarp();
+                return true;
+            };
+            const bool requester = dyn && crank == 0;
+            Cursor cur = cursor0;
+            for (int j = 0; ok; ++j) {
+                Work w;
+                const int g = get_work(cur, w);
+                if (g <= 0) {
+                    ok = g == 0;
+                    break;
+                }
+                // the last item of a list: ask for the next list now
+                if (requester && cur.pos == cur.len && !(ok = request(cur.resp))) break;
                 int a_row, b_row, bt;
                 operand_rows(w.tile, a_row, b_row, bt);
                 const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;   // batch coordinates
@@ -493,6 +606,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
             GEMM_TR_SET(kTrEmptyWaitNs, empty_wait_ns);
+            if (lane == 0) GEMM_TR_SET(kTrClcWaitProducerNs, clc_wait_ns);
             (void)empty_wait_ns;
             // Every slot's last use must be released (the MMA's commit arrives
             // on this CTA's empty barriers) before the CTA may exit.
@@ -516,7 +630,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             bool ok = true;
             int i = 0;
             uint64_t full_wait_ns = 0, acc_wait_ns = 0;   // trace builds only
-            const int nwork = work_count(p.sched, pair_id);
             if (p.stall_test) {
                 // A wait that cannot end: fix_bar(0) gets no arrival unless a
                 // stream-K finisher uses it, and this launch has none.  It runs
@@ -524,8 +637,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // timeout path (status, abort flag, orderly teardown).
                 ok = __all_sync(0xffffffffu, wait_bounded<false>(fix_bar(0), 0, abort_flag, p, kRoleStallTest, 0));
             }
-            for (; i < nwork && ok; ++i) {
-                const Work w = work_item(p.sched, pair_id, i);
+            Cursor cur = cursor0;
+            for (; ok; ++i) {
+                Work w;
+                const int g = get_work(cur, w);
+                if (g <= 0) {
+                    ok = g == 0;
+                    break;
+                }
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
                 const uint64_t ta = GEMM_TR_NOW();
                 if (!__all_sync(0xffffffffu, wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i))) {
@@ -578,6 +697,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             GEMM_TR(kTrWorkItems);
             GEMM_TR_SET(kTrFullWaitNs, full_wait_ns);
             GEMM_TR_SET(kTrAccEmptyWaitNs, acc_wait_ns);
+            if (lane == 0) GEMM_TR_SET(kTrClcWaitMmaNs, clc_wait_ns);
             (void)full_wait_ns;
             (void)acc_wait_ns;
             // Both accumulators must be released by every epilogue warp of the
@@ -631,12 +751,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         };
 
-        const int nwork = work_count(p.sched, pair_id);
-        for (int i = 0; i < nwork; ++i) {
-            const Work w = work_item(p.sched, pair_id, i);
+        Work w, nw;
+        Cursor cur = cursor0;
+        int g = get_work(cur, w), gn = 0;
+        for (int i = 0; g > 0; ++i) {
             const uint32_t b = i & 1, aphase = (i >> 1) & 1;
             const bool got = wait_bounded<false>(accf_bar(b), aphase, abort_flag, p, 5, i);
             if (!__all_sync(0xffffffffu, got)) break;
+            // The next item now: whether this tile is the unit's last decides
+            // how it is stored.
+            gn = get_work(cur, nw);
+            if (gn < 0) break;
             if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiStart, i);
             tc_fence_after_sync();
             int bt, mt, nt;
@@ -644,7 +769,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int row0 = mt * C::kTileM + (int)crank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
-            if (w.ncontrib == 1 && i == nwork - 1) {
+            if (w.ncontrib == 1 && gn == 0) {
                 // The unit's last tile: nothing overlaps its epilogue, and its
                 // operand ring is idle (no later loads, every MMA done), so each
                 // chunk gets its own box there, one fence covers them all and
@@ -763,12 +888,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if constexpr (kPair == 2) mbar_arrive_cluster(map_shared_rank(acce_bar(b), leader));
                 else mbar_arrive_local(acce_bar(b));
             }
+            w = nw;
+            g = gn;
         }
         // Only the staging buffers' reads must be done before shared memory
         // goes away; the writes to C complete with the grid.
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
         if (warp == 2 && lane == 0) GEMM_TR(kTrEpiDone);
+        if (warp == 2 && lane == 0) GEMM_TR_SET(kTrClcWaitEpiNs, clc_wait_ns);
     }
 
     // ---- teardown

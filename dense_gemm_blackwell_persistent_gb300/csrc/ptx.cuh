@@ -92,6 +92,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
 }
+// Arrive with expected transaction bytes on a barrier that may live in
+// another CTA of the cluster (`cluster_bar` from map_shared_rank).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -115,6 +122,40 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel one cluster of this grid that has not started
+// yet, so that the caller can do its work instead.  The 16-byte response
+// lands at `resp` and completes 16 transaction bytes on `bar`; with
+// kMulticast, at the same offsets in every CTA of the issuing cluster.
+template <bool kMulticast>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    if constexpr (kMulticast)
+        asm volatile(
+            "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128"
+            " [%0], [%1];" ::"r"(resp), "r"(bar)
+            : "memory");
+    else
+        asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+                     ::"r"(resp), "r"(bar)
+                     : "memory");
+}
+// Read a response: the x index of the first CTA of the cancelled cluster,
+// or -1 when the request found no cluster left to cancel.
+__device__ __forceinline__ int clc_response(uint32_t resp) {
+    uint32_t ok, x = 0;
+    asm volatile(
+        "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t.reg .b64 lo, hi;\n\t"
+        "ld.shared.v2.b64 {lo, hi}, [%2];\n\t"
+        "mov.b128 h, {lo, hi};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok ? (int)x : -1;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -127,19 +127,23 @@ GB300_HD int work_count(const Schedule& s, int u) {
     return s.dp_waves + (q1 - q0 + 1);
 }
 
+// All `kb` k-blocks of tile `tile`, by one unit.
+GB300_HD Work whole_tile(int tile, int kb) {
+    Work w;
+    w.tile = tile;
+    w.kb_begin = 0;
+    w.kb_end = kb;
+    w.contrib = 0;
+    w.ncontrib = 1;
+    w.slot = -1;
+    w.sk_index = -1;
+    return w;
+}
+
 // The j-th work item of unit u (0 <= j < work_count(s, u)).
 GB300_HD Work work_item(const Schedule& s, int u, int j) {
+    if (j < s.dp_waves || s.sk_tiles == 0) return whole_tile(u + j * s.units, s.kb);
     Work w;
-    if (j < s.dp_waves || s.sk_tiles == 0) {
-        w.tile = u + j * s.units;
-        w.kb_begin = 0;
-        w.kb_end = s.kb;
-        w.contrib = 0;
-        w.ncontrib = 1;
-        w.slot = -1;
-        w.sk_index = -1;
-        return w;
-    }
     const int64_t b0 = sk_begin(s, u), b1 = sk_begin(s, u + 1);
     const int q = (int)(b0 / s.kb) + (j - s.dp_waves);
     const int64_t tile_lo = (int64_t)q * s.kb, tile_hi = tile_lo + s.kb;

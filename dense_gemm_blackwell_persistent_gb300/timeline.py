@@ -21,15 +21,16 @@ import json
 import numpy as np
 import torch
 
-from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_MAX_CTAS, GEMM_OPT_MULTICAST, GEMM_OPT_STREAM_K, GEMM_OPT_TILE_N,
-               VARIANT,
+from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_DYNAMIC, GEMM_OPT_MAX_CTAS, GEMM_OPT_MULTICAST, GEMM_OPT_STREAM_K,
+               GEMM_OPT_TILE_N, VARIANT,
                gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_last_launch, gemm_plan_run,
                gemm_plan_set_option, gemm_plan_trace)
 
 POINTS = {0: "entry", 3: "first_full", 11: "epilogue_stores_done", 4: "teardown", 12: "cluster_arrived",
           13: "cluster_done", 14: "tmem_dealloc", 5: "exit"}
 ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published", 48: "reduce_done"}
-TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us"}
+TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us",
+          1: "producer_wait_response_us", 10: "mma_wait_response_us", 2: "epilogue_wait_response_us"}
 PROLOGUE = {1: "barriers_initialised", 2: "tensormaps_prefetched", 3: "cluster_arrived", 4: "cluster_passed",
             5: "first_item_decoded", 6: "first_slot_free", 7: "first_loads_issued", 8: "mma_warp_has_tmem"}
 
@@ -97,6 +98,7 @@ def main():
     ap.add_argument("--pair", type=int, default=2)
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stream-k", type=int, default=0)
+    ap.add_argument("--dynamic", type=int, default=0, help="1: tiles handed out at run time")
     ap.add_argument("--multicast", type=int, default=-1, help="-1 auto, 0 off, 1 on")
     ap.add_argument("--max-ctas", type=int, default=0)
     ap.add_argument("--no-flush", action="store_true", help="keep the operands in L2 before the traced launch")
@@ -109,6 +111,7 @@ def main():
     gemm_plan_set_option(plan, GEMM_OPT_CTA_PAIR, a.pair)
     gemm_plan_set_option(plan, GEMM_OPT_TILE_N, a.tile_n)
     gemm_plan_set_option(plan, GEMM_OPT_STREAM_K, a.stream_k)
+    gemm_plan_set_option(plan, GEMM_OPT_DYNAMIC, a.dynamic)
     gemm_plan_set_option(plan, GEMM_OPT_MULTICAST, a.multicast)
     gemm_plan_set_option(plan, GEMM_OPT_MAX_CTAS, a.max_ctas)
     tin = torch.bfloat16 if a.dtype == 0 else torch.float16

@@ -112,11 +112,27 @@ typedef enum {
                                     rows of A and B are not a multiple of 128 bytes   */
     GEMM_OPT_WAIT_LIMIT_US = 7,  /* bound on any single wait inside the kernel, in µs,
                                     1..60e6 (0 = default: 2 s)                         */
-    GEMM_OPT_STALL_TEST = 8      /* tests of the timeout path only: 1 = the MMA warp
+    GEMM_OPT_STALL_TEST = 8,     /* tests of the timeout path only: 1 = the MMA warp
                                     first waits on a barrier nothing completes, so the
                                     run ends, after about two wait bounds, with
                                     GEMM_ERR_TIMEOUT (role 8) in the status word and
                                     C unwritten; 0 (default) = off                     */
+    GEMM_OPT_DYNAMIC = 9         /* run-time tile scheduling through cluster launch
+                                    control ("Writing Mosaic GPU kernels with Pallas",
+                                    "Cluster launch control"): the grid gets one
+                                    cluster per list of tiles, and a unit that has
+                                    done its list takes over the list of a cluster
+                                    that has not started, so faster SMs do more
+                                    tiles.  1: the persistent units keep their whole
+                                    waves and each tile of a partial last wave is a
+                                    list of its own (no effect when the tiles fill
+                                    whole waves or fit in one); 2: every tile is a
+                                    list.  Whole tiles only (overrides
+                                    GEMM_OPT_STREAM_K).  0: the static persistent
+                                    schedule.  -1 (default): 1 from six whole waves
+                                    of tiles on (where it measured faster), else 0;
+                                    0 on plans with GEMM_OPT_MAX_CTAS or
+                                    GEMM_OPT_STREAM_K set                          */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan
@@ -190,7 +206,9 @@ int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);
 
 /* Launch configuration of the last run on this plan (for reports): CTAs
  * launched, CTAs per work unit (1, 2 or 4), tile width, whole-tile waves and
- * the number of tiles split along K by the stream-K tail. */
+ * the number of tiles split along K by the stream-K tail.  A run with a
+ * dynamic work list reports its grid (one unit per list) and the whole
+ * waves of the persistent units (0 when every tile is a list). */
 int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* tile_n, int* dp_waves,
                           int* sk_tiles);
 

@@ -186,19 +186,25 @@ def test_every_tile_width(g, fresh_plan, unit, tile_n):
         parity.assert_within(C, C_ref, S, out, f"tile_n={tile_n} pair={pair} out={out}")
 
 
-@pytest.mark.parametrize("name,expect", [("gemm_4096_bf16", 224), ("gemm_1024x4096x4096_f16", 224),
-                                         ("gemm_8192_bf16", 256)])
-def test_tile_width_choice_fills_waves(g, plan, name, expect):
-    """The host picks the width that minimises waves × (width + 48): a
-    narrower tile when it turns a partial last wave into whole waves."""
+@pytest.mark.parametrize("name,expect", [("gemm_4096_bf16", (224, 152, 4)),
+                                         ("gemm_1024x4096x4096_f16", (224, 152, 1)),
+                                         ("gemm_8192_bf16", (256, 224, 13))])
+def test_default_launch_of_workloads(g, fresh_plan, name, expect):
+    """Tile width: the candidate with the fewest waves × measured cycles per
+    k-block, so a narrower tile where it turns a partial last wave into
+    whole waves.  Schedule: static where the tiles fill whole waves (4096³:
+    304 tiles = 4 waves on 76 pairs); at 8192³ (1024 tiles = 13 waves + 36)
+    the 76 persistent pairs keep 13 waves each and the 36 tiles of the
+    partial wave are handed out at run time (76 + 36 clusters of 2 CTAs)."""
     w = wl.WORKLOADS[name]
     A = torch.zeros((w.M, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
     B = torch.zeros((w.N, w.K), dtype=wl.TORCH_DTYPES[w.dtype], device="cuda")
-    C = run(g, plan, A, B, w.out_dtype)
+    C = run(g, fresh_plan, A, B, w.out_dtype)
     assert bool((C == 0).all())
-    launch = g.gemm_plan_last_launch(plan)
-    if launch["ctas"] == 152 and launch["ctas_per_unit"] == 2:
-        assert launch["tile_n"] == expect, launch
+    launch = g.gemm_plan_last_launch(fresh_plan)
+    assert launch["ctas_per_unit"] == 2, launch
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (launch["tile_n"], launch["ctas"], launch["dp_waves"]) == expect, launch
 
 
 # (M, N, K, tile width, {CTAs per unit: CTA cap}): shapes whose schedule
@@ -251,6 +257,94 @@ def test_stream_k_off_matches_within_tolerance(g, fresh_plan):
     C_ref, S = oracle_full(A, B)
     parity.assert_within(C_on, C_ref, S, wl.F32, "stream-K on")
     parity.assert_within(C_off, C_ref, S, wl.F32, "stream-K off")
+
+
+# ------------------------------------------------------------------ dynamic tile scheduling
+
+# (M, N, K, tile width): several tiles per resident unit, ragged edges and a
+# partial last k-block; one-k-block tiles, so that units come back for work
+# quickly and the response ring wraps many times.  With every resident unit
+# (152 CTAs as singles or pairs, 144 in 4-CTA clusters) the tile counts leave
+# a partial last wave, and the first case fits in one wave.
+DYNAMIC_CASES = [
+    (1300, 1096, 520, 224),
+    (2048, 2048, 264, 128),
+    (4096, 4096, 64, 128),
+]
+
+
+def tiles_of(M, N, unit, tile_n, batch=1):
+    return batch * (-(-M // (128 * unit))) * (-(-N // tile_n))
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["tail", "every_tile"])
+@pytest.mark.parametrize("unit", UNITS)
+@pytest.mark.parametrize("case", DYNAMIC_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_dynamic_schedule(g, fresh_plan, unit, case, mode):
+    """Clusters that finish their list of tiles take over the lists of
+    clusters that have not started (cluster launch control).  Every tile
+    must be computed exactly once: integer inputs give the oracle's exact
+    sums."""
+    M, N, K, tile_n = case
+    configure(g, fresh_plan, unit)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, tile_n)
+    T = tiles_of(M, N, unit, tile_n)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, 0)
+    A, B = draw(M, N, K, dist="int", seed=K + 2)
+    C_ref, _ = oracle_full(A, B)
+    Ad, Bd = A.cuda(), B.cuda()
+    run(g, fresh_plan, Ad, Bd, wl.F32)
+    static = g.gemm_plan_last_launch(fresh_plan)
+    P = static["ctas"] // unit   # resident units (or the tiles, if fewer)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, mode)
+    for out in OUTS:
+        C = parity.to_f64(run(g, fresh_plan, Ad, Bd, out))
+        launch = g.gemm_plan_last_launch(fresh_plan)
+        if mode == 2:
+            assert (launch["ctas"], launch["dp_waves"]) == (T * unit, 0), launch
+        elif T > P and T % P:
+            assert (launch["ctas"], launch["dp_waves"]) == ((P + T % P) * unit, T // P), (launch, T, P)
+        else:
+            assert launch == static, (launch, static)
+        want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+        assert np.array_equal(C, want), f"dynamic {case} unit={unit} out={out}: {int((C != want).sum())} mismatches"
+    A, B = draw(M, N, K, dtype=wl.BF16, seed=K * 5 + 1)
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), wl.BF16)), C_ref, S, wl.BF16,
+                         f"dynamic {case} unit={unit}")
+
+
+@pytest.mark.parametrize("unit", UNITS)
+def test_dynamic_batched_and_fp8(g, fresh_plan, unit):
+    configure(g, fresh_plan, unit)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, 2)
+    case = (5, 520, 776, 1008, False, False, 0, 0)
+    As, Bs = draw_batch(case, "int", seed=40 + unit)
+    Cs = run_batched(g, fresh_plan, As, Bs, case, wl.F32)
+    assert g.gemm_plan_last_launch(fresh_plan)["dp_waves"] == 0
+    for e in range(case[0]):
+        C_ref, _ = oracle_full(As[e].contiguous(), Bs[e].contiguous())
+        assert np.array_equal(parity.to_f64(Cs[e]), C_ref), f"batch element {e}"
+    A, B = draw(1100, 1096, 1024, dtype=wl.E4M3, dist="int", seed=41)
+    C = parity.to_f64(run(g, fresh_plan, A.cuda(), B.cuda(), wl.F32))
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(C, C_ref)
+
+
+def test_dynamic_and_static_agree(g, fresh_plan):
+    """The schedule decides only where a tile is computed, not how: the
+    same inputs give bitwise the same C every way."""
+    M, N, K = 3000, 2800, 1000
+    A, B = draw(M, N, K, seed=43)
+    Ad, Bd = A.cuda(), B.cuda()
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, 0)
+    C_sta = run(g, fresh_plan, Ad, Bd, wl.F32)
+    for mode in (1, 2):
+        g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, mode)
+        C_dyn = run(g, fresh_plan, Ad, Bd, wl.F32)
+        assert torch.equal(C_dyn, C_sta), f"mode {mode}"
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(parity.to_f64(C_dyn), C_ref, S, wl.F32, "dynamic")
 
 
 # ------------------------------------------------------------------ 8-bit float inputs
@@ -630,8 +724,9 @@ def test_error_codes(g, plan):
     assert g.gemm_plan_status(plan) == 0
 
 
+@pytest.mark.parametrize("dynamic", [0, 2], ids=["static", "dynamic"])
 @pytest.mark.parametrize("unit", UNITS)
-def test_bounded_wait_expires_and_plan_recovers(g, fresh_plan, unit):
+def test_bounded_wait_expires_and_plan_recovers(g, fresh_plan, unit, dynamic):
     """Failure detection without a GPU fault: with the test option on, the MMA
     warp waits on a barrier nothing completes.  The wait runs out after the
     shortened bound, the kernel records GEMM_ERR_TIMEOUT, the other roles
@@ -639,6 +734,7 @@ def test_bounded_wait_expires_and_plan_recovers(g, fresh_plan, unit):
     CTAs tear down in order, and the same plan then computes correctly."""
     import time
     configure(g, fresh_plan, unit)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, dynamic)
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_WAIT_LIMIT_US, 20000)   # 20 ms
     g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_STALL_TEST, 1)
     A, B = draw(512, 520, 512, dist="int", seed=9)
