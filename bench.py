@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (0 = library choice)")
     ap.add_argument("--multicast", type=int, default=-1, help="-1 auto, 0 off, 1 on (CTA pairs only)")
     ap.add_argument("--stream-k", type=int, default=0, help="1: stream-K tail")
+    ap.add_argument("--dynamic", type=int, default=-1, help="-1 auto, 0 static, 1 hand out the partial wave, 2 every tile")
+    ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core issue-rate probe")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     return ap.parse_args()
 
@@ -282,6 +284,7 @@ def main():
     plan = g.gemm_plan_create(local)
     if args.cta_pair:
         g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, args.cta_pair)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_DYNAMIC, args.dynamic)
     if args.group_m:
         g.gemm_plan_set_option(plan, g.GEMM_OPT_GROUP_M, args.group_m)
     if args.tile_n:
@@ -377,6 +380,20 @@ def main():
         except RuntimeError as e:   # a torch build without this fp8 path: no reference line
             extra["cublas_reference"] = {"unavailable": str(e).splitlines()[0][:200]}
 
+    # Context for the roofline: the tensor cores' own rate, measured by a
+    # stream of back-to-back MMAs of this kernel's shape with no loads, on
+    # every SM, right after the timed region (outside it).
+    mma_probe = None
+    if rank == 0 and not args.no_probe:
+        r = g.gemm_probe_mma_rate(w.dtype, args.cta_pair or 2, 1 << 16)
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        mma_probe = {"tflops": r["tflops"], "sm_mhz": r["sm_mhz"], "flop_per_clk_per_sm": r["flop_per_clk_per_sm"],
+                     "frac": achieved / r["tflops"],
+                     "peak_at_max_clock_tflops":
+                         r["flop_per_clk_per_sm"] * sms * float(peaks.get("sm_max_mhz", 2070.0)) / 1e6,
+                     "how": "gemm_probe_mma_rate: 65536 back-to-back tcgen05.mma per SM, operands in shared memory, "
+                            "no loads; frac = achieved / tflops"}
+
     e2e = None
     if not args.no_e2e:
         Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
@@ -416,7 +433,7 @@ def main():
                        "vs_baseline_ref": "pages' 293.6 TFLOP/s, Mojo part-2 kernel 4 on B200 (context)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": peak_note},
+                         "peak_source": peak_note, "mma_probe": mma_probe},
             "clocks": clocks,
             "gpu_launches": args.steps,
             "e2e": e2e,

@@ -1,7 +1,8 @@
 """Build the CUDA library in-tree with nvcc (sm_103a only).
 
 Produces ``dense_gemm_blackwell_persistent_gb300/_lib/libgb300gemm.so`` from
-``csrc/gemm_api.cu`` (host side) and 24 objects of ``csrc/kernels_inst.cu``
+``csrc/gemm_api.cu`` (host side), ``csrc/mma_probe.cu`` (the tensor-core
+issue-rate probe) and 24 objects of ``csrc/kernels_inst.cu``
 (one per unit size × output type × operand width, plus the padded MN-major-B
 forms), compiled in parallel.  The CUDA
 runtime is linked statically and the driver's tensor-map encoder is looked up
@@ -86,7 +87,8 @@ def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
     common = [nvcc, *NVCC_FLAGS, *VARIANT_DEFINES[variant], "-I", INCLUDE, "-I", CSRC, "-c"]
     if verbose:
         common.insert(1, "-Xptxas=-v")
-    jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose)]
+    jobs = [(common + [os.path.join(CSRC, "gemm_api.cu"), "-o", os.path.join(objdir, "gemm_api.o")], verbose),
+            (common + [os.path.join(CSRC, "mma_probe.cu"), "-o", os.path.join(objdir, "mma_probe.o")], verbose)]
     for cluster, out, inp, pad in VARIANTS:
         obj = os.path.join(objdir, f"kernels_c{cluster}_o{out}_i{inp}_p{pad}.o")
         jobs.append((common + [f"-DGEMM_INST_CLUSTER={cluster}", f"-DGEMM_INST_OUT={out}", f"-DGEMM_INST_IN={inp}",

@@ -63,7 +63,7 @@ namespace gb300 {
 // %globaltimer stamps, wait totals and SM cycle counts in a device buffer of
 // kTraceSlots 64-bit words per CTA.  Without GEMM_TRACE the macros compile
 // to nothing.
-constexpr int kTraceSlots = 80;
+constexpr int kTraceSlots = 88;
 enum TraceSlot {
     kTrEntry = 0,         // %globaltimer at entry (thread 0; written at teardown)
     kTrClcWaitProducerNs = 1, kTrClcWaitEpiNs = 2,   // dynamic work list: time waiting for responses
@@ -83,6 +83,7 @@ enum TraceSlot {
     kTrClkMmaEnd = 56,    // ... and at mma_end + item: cycles per k-block
     kTrClkPro = 64,       // + 0..8: SM cycles at the prologue steps (see timeline.PROLOGUE)
     kTrDynTile = 72,      // + 1 + r (r < 7): the list (cluster) that response r handed to this unit
+    kTrSmid = 80,         // %smid of the CTA, + 1
 };
 #ifdef GEMM_TRACE
 #define GEMM_TR_ON() (p.trace && blockIdx.x < (unsigned)p.trace_ctas)
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (threadIdx.x == 0) {
         GEMM_TR_CLK(0);
         tr_entry_ns = global_timer_ns();
+        GEMM_TR_SET(kTrSmid, (unsigned long long)sm_id() + 1);
     }
 #endif
     const uint32_t base = smem_addr(smem_raw);

@@ -250,6 +250,25 @@ int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N
                      int dtype, int out_dtype, void* stream);
 
 /* Static text for a status code. */
+/* Tensor-core issue-rate probe (a measurement, not part of a product):
+ * on the current device every SM holds one CTA (cta_pair = 1) or one CTA of
+ * a pair (cta_pair = 2), and one thread per CTA (pair) issues
+ * `mmas_per_sm` back-to-back tcgen05.mma of the GEMM kernel's shape --
+ * 128×256 per CTA, K = 16 (dtype GEMM_BF16/GEMM_F16) or 32 (GEMM_E4M3/
+ * GEMM_E5M2) -- from operand tiles already in shared memory: no loads, no
+ * epilogue.  The ceiling a GEMM's K loop can reach, measured ("Optimizing
+ * Blackwell Matrix Multiplication in Mojo (Part 2)" rates its kernels
+ * against the tensor cores' peak).  Outputs, any of which may be NULL:
+ * the dense FLOP per SM clock (median over CTAs, from the SM cycle
+ * counter), the TFLOP/s of all SMs together (CUDA events around the
+ * launch) and the SM clock in MHz during the stream (cycles ÷ %globaltimer
+ * ns, median).  `mmas_per_sm`: a multiple of 4 in [4, 2^24].  Synchronous:
+ * allocates and frees a few KB of device memory and waits for the device.
+ * Errors: GEMM_ERR_INVALID_ARG, GEMM_ERR_NO_DEVICE, GEMM_ERR_CUDA,
+ * GEMM_ERR_TIMEOUT (a completion wait ran out after 10 s). */
+int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm, double* flop_per_clk_per_sm,
+                        double* tflops, double* sm_mhz);
+
 const char* gemm_strerror(int status);
 
 #ifdef __cplusplus

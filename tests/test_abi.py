@@ -81,6 +81,10 @@ def test_host_validation_without_gpu(lib):
     assert rs("gemm_plan_destroy", None) == lib.GEMM_ERR_INVALID_ARG
     assert rs("gemm_plan_set_option", None, 1, ctypes.c_int64(2)) == lib.GEMM_ERR_INVALID_ARG
     assert rs("gemm_plan_create", None, -1, 0) == lib.GEMM_ERR_INVALID_ARG
+    # the tensor-core probe checks its arguments before touching the device
+    assert rs("gemm_probe_mma_rate", 2, 2, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG   # fp32 operands
+    assert rs("gemm_probe_mma_rate", 0, 4, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG   # 4 CTAs
+    assert rs("gemm_probe_mma_rate", 0, 2, 6, None, None, None) == lib.GEMM_ERR_INVALID_ARG         # not whole k-blocks
     for code in range(-8, 1):
         assert lib.gemm_strerror(code) != "unknown status"
 
@@ -96,6 +100,7 @@ def test_no_device_is_reported(lib):
     good = vp(1 << 20)
     # a well-formed call with no device: fails cleanly, enqueues nothing
     assert lib.raw_status("gemm_run", good, good, good, 64, 64, 64, 0, 2, None) == lib.GEMM_ERR_NO_DEVICE
+    assert lib.raw_status("gemm_probe_mma_rate", 0, 2, 1 << 12, None, None, None) == lib.GEMM_ERR_NO_DEVICE
 
 
 def test_product_path_has_no_cpu_fallback():

@@ -347,6 +347,31 @@ def test_dynamic_and_static_agree(g, fresh_plan):
     parity.assert_within(parity.to_f64(C_dyn), C_ref, S, wl.F32, "dynamic")
 
 
+# ------------------------------------------------------------------ tensor-core issue-rate probe
+
+@pytest.mark.parametrize("dtype,nominal", [(wl.BF16, 8192), (wl.F16, 8192), (wl.E4M3, 16384), (wl.E5M2, 16384)],
+                         ids=["bf16", "f16", "e4m3", "e5m2"])
+@pytest.mark.parametrize("pair", [2, 1])
+def test_mma_probe_rate(g, dtype, nominal, pair):
+    """Back-to-back MMAs with no loads run at the tensor cores' dense rate:
+    8192 FLOP per SM clock for 16-bit operands and twice that for 8-bit
+    ones (NVIDIA's dense figures divided by SMs × clock), and the all-SM
+    rate agrees with that rate × SMs × the clock measured alongside."""
+    r = g.gemm_probe_mma_rate(dtype, pair, 1 << 16)
+    assert abs(r["flop_per_clk_per_sm"] / nominal - 1) < 0.02, r
+    assert 300 < r["sm_mhz"] < 2200, r
+    sms = torch.cuda.get_device_properties(0).multi_processor_count // pair * pair
+    expect = r["flop_per_clk_per_sm"] * sms * r["sm_mhz"] * 1e6 / 1e12
+    assert 0.8 < r["tflops"] / expect < 1.1, (r, expect)
+
+
+def test_mma_probe_arguments(g):
+    import ctypes
+    d = ctypes.c_double()
+    for args in ((wl.F32, 2, 1 << 12), (wl.BF16, 3, 1 << 12), (wl.BF16, 2, 6), (wl.BF16, 2, 0), (wl.BF16, 2, 1 << 25)):
+        assert g.raw_status("gemm_probe_mma_rate", *args, ctypes.byref(d), None, None) == g.GEMM_ERR_INVALID_ARG
+
+
 # ------------------------------------------------------------------ 8-bit float inputs
 
 @pytest.mark.parametrize("unit", UNITS)
