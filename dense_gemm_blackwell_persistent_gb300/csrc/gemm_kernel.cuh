@@ -1,8 +1,10 @@
 // gemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
-// C[M×N] = A[M×K] · B[N×K]ᵀ, bf16/f16 in, fp32 accumulate in TMEM, C out as
-// fp32/bf16/f16.  One CTA (or one CTA pair) stays resident per SM (pair of
-// SMs) and walks a static list of output tiles.
+// C[M×N] = A[M×K] · B[N×K]ᵀ, bf16/f16 (or 8-bit float) in, fp32 accumulate
+// in TMEM, C out as fp32/bf16/f16.  One CTA (or one CTA pair) stays resident
+// per SM (pair of SMs) and walks a list of output tiles: a static list, or
+// one that grows at run time through cluster launch control (the tiles of
+// clusters that have not started).
 //
 // Roles inside a CTA (192 threads):
 //   warp 0      TMA producer: fills a kStages-deep shared-memory ring with

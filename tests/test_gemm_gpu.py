@@ -331,6 +331,22 @@ def test_dynamic_batched_and_fp8(g, fresh_plan, unit):
     assert np.array_equal(C, C_ref)
 
 
+def test_dynamic_by_default_on_many_waves(g, fresh_plan):
+    """With default options, a product of 6 or more whole waves and a
+    partial one hands the partial wave out at run time: here 32 batched
+    1024×1024×128 products, 512 tiles of 256×256 on 76 pairs = 6 waves + 56
+    tiles, so 76 + 56 clusters.  Every element exact for integer inputs."""
+    case = (32, 1024, 1024, 128, False, False, 0, 0)
+    As, Bs = draw_batch(case, "int", seed=45)
+    Cs = run_batched(g, fresh_plan, As, Bs, case, wl.F32)
+    launch = g.gemm_plan_last_launch(fresh_plan)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (launch["ctas"], launch["tile_n"], launch["dp_waves"]) == ((76 + 56) * 2, 256, 6), launch
+    for e in range(case[0]):
+        C_ref, _ = oracle_full(As[e].contiguous(), Bs[e].contiguous())
+        assert np.array_equal(parity.to_f64(Cs[e]), C_ref), f"batch element {e}"
+
+
 def test_dynamic_and_static_agree(g, fresh_plan):
     """The schedule decides only where a tile is computed, not how: the
     same inputs give bitwise the same C every way."""
