@@ -14,7 +14,6 @@ from __future__ import annotations
 
 import random
 
-import numpy as np
 import pytest
 import torch
 
@@ -25,7 +24,6 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 CASES = 96
-CODE_OF = {t: code for code, t in wl.TORCH_DTYPES.items()}
 
 
 def make_case(i: int) -> dict:
