@@ -230,13 +230,14 @@ def pin_rank1(o):
 
 
 def pin_bruteforce_exact(o):
-    # Every shape 1..4 in each of M, N, K: the exact rational sum, rounded once,
-    # must equal the oracle (fp64 sums of these bf16/f16 products are exact).
+    # Every shape 1..8 in each of M, N, K (512 shapes): the exact rational sum,
+    # rounded once, must equal the oracle (fp64 sums of up to eight products
+    # of these N(0,1)-drawn bf16/f16 values are exact).
     rng = np.random.default_rng(3)
     for dt in (BF16, F16):
-        for M in range(1, 5):
-            for N in range(1, 5):
-                for K in range(1, 5):
+        for M in range(1, 9):
+            for N in range(1, 9):
+                for K in range(1, 9):
                     A = _rand_bits(rng, (M, K), dt)
                     B = _rand_bits(rng, (N, K), dt)
                     a, b = o.decode(A, dt), o.decode(B, dt)
