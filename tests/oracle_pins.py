@@ -287,6 +287,20 @@ def pin_power_of_two_scaling(o):
     assert np.array_equal(C2, 4.0 * C1)
 
 
+def pin_linearity_in_a(o):
+    # C(A1 + A2, B) = C(A1, B) + C(A2, B): small integers, so every operand,
+    # product and sum is exact in bf16/fp64 and the identity holds bit for bit.
+    rng = np.random.default_rng(7)
+    x1 = rng.integers(-8, 9, size=(13, 41)).astype(np.float64)
+    x2 = rng.integers(-8, 9, size=(13, 41)).astype(np.float64)
+    B = _bits_of(rng.integers(-8, 9, size=(17, 41)), BF16)
+    C1, _ = o.gemm(_bits_of(x1, BF16), B, BF16)
+    C2, _ = o.gemm(_bits_of(x2, BF16), B, BF16)
+    C12, _ = o.gemm(_bits_of(x1 + x2, BF16), B, BF16)
+    assert np.array_equal(C12, C1 + C2)
+    assert np.abs(C1).max() > 0 and not np.array_equal(C1, C2)
+
+
 def pin_special_values(o):
     # IEEE: inf·positive = inf, inf·0 = NaN, NaN propagates.
     A = _bits_of(np.array([[np.inf, 1.0], [1.0, np.nan], [1.0, 1.0]]), BF16)
@@ -384,7 +398,7 @@ ALL_PINS = [
     pin_decode_golden, pin_decode_all_f16_vs_numpy, pin_decode_all_bf16_vs_torch,
     pin_encode_vs_numpy_f16, pin_encode_vs_torch_bf16, pin_worked_example, pin_identity,
     pin_all_ones, pin_rank1, pin_bruteforce_exact, pin_numpy_float64, pin_swap_symmetry,
-    pin_power_of_two_scaling, pin_special_values, pin_empty_sizes, pin_entries_agree,
+    pin_power_of_two_scaling, pin_linearity_in_a, pin_special_values, pin_empty_sizes, pin_entries_agree,
     pin_decode_fp8_golden, pin_decode_all_fp8_vs_torch, pin_fp8_bruteforce,
     pin_fp8_matches_bf16_on_shared_values, pin_fp8_entries_agree,
 ]
