@@ -347,6 +347,43 @@ def test_dynamic_by_default_on_many_waves(g, fresh_plan):
         assert np.array_equal(parity.to_f64(Cs[e]), C_ref), f"batch element {e}"
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["tail", "every_tile"])
+def test_dynamic_schedule_in_cuda_graph(g, fresh_plan, mode):
+    """A run with a dynamic work list recorded into a CUDA graph: each replay
+    launches the grid again and the running clusters cancel the ones that
+    have not started, so every replay must compute every tile once.
+    2048×4096×64 with 256×128 pair tiles is 256 tiles (3 waves + 28 on 76
+    pairs: 104 or 256 clusters launched); replays on new integer inputs must
+    equal the oracle exactly."""
+    M, N, K = 2048, 4096, 64
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_TILE_N, 128)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_DYNAMIC, mode)
+    Ad = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    Bd = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                        s.cuda_stream)
+    s.synchronize()
+    assert g.gemm_plan_last_launch(fresh_plan)["ctas"] > 152 or \
+        torch.cuda.get_device_properties(0).multi_processor_count != 152
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                        torch.cuda.current_stream().cuda_stream)
+    for seed in (51, 52):
+        A, B = draw(M, N, K, dist="int", seed=seed)
+        Ad.copy_(A)
+        Bd.copy_(B)
+        Cd.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g.gemm_plan_status(fresh_plan) == 0
+        C_ref, _ = oracle_full(A, B)
+        assert np.array_equal(parity.to_f64(Cd), C_ref), f"replay with seed {seed}"
+
+
 def test_dynamic_and_static_agree(g, fresh_plan):
     """The schedule decides only where a tile is computed, not how: the
     same inputs give bitwise the same C every way."""
@@ -730,6 +767,20 @@ def test_m_or_n_zero_is_noop(g, plan):
     g.gemm_plan_run(plan, A.data_ptr(), A.data_ptr(), sentinel.data_ptr(), 16, 0, 64, 0, 2, 0)
     torch.cuda.synchronize()
     assert bool((sentinel == 7.0).all())
+
+
+@pytest.mark.parametrize("unit", UNITS)
+def test_all_ones_ragged_is_k(g, fresh_plan, unit):
+    """All-ones operands on a shape that is a multiple of no tile and of no
+    k-block: every C[i,j] must be exactly K.  Out-of-bounds rows, columns and
+    K elements of the last boxes arrive as zeros (TMA zero fill) and add
+    nothing; any garbage there would show."""
+    configure(g, fresh_plan, unit)
+    for M, N, K, out in ((1000, 1096, 1000, wl.F32), (517, 264, 72, wl.BF16), (130, 1992, 4104, wl.F32)):
+        A = torch.ones((M, K), dtype=torch.bfloat16, device="cuda")
+        B = torch.ones((N, K), dtype=torch.bfloat16, device="cuda")
+        C = run(g, fresh_plan, A, B, out).float()
+        assert bool((C == K).all()), f"{M}x{N}x{K} unit={unit}: {int((C != K).sum())} entries differ from K"
 
 
 def test_rows_beyond_m_untouched(g, plan):
