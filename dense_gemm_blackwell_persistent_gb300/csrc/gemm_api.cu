@@ -327,7 +327,10 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     // cancelled by running ones, which do their lists).
     const int resident = resident_units(plan, cluster);
     int dyn_units = 0, dyn_waves = 0;
-    const bool dyn = dynamic_lists(plan, p.num_tiles, resident, &dyn_units, &dyn_waves);
+    bool dyn = dynamic_lists(plan, p.num_tiles, resident, &dyn_units, &dyn_waves);
+    // one cluster per list: keep the grid within the launch limit (x < 2^31), else stay static
+    if (dyn && ((int64_t)dyn_units + (p.num_tiles - (int64_t)dyn_units * dyn_waves)) * cluster >= (int64_t(1) << 31))
+        dyn = false;
     const bool sk = !dyn && plan->stream_k && plan->d_partials != nullptr && plan->d_flags != nullptr;
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
     p.dynamic = dyn ? 1 : 0;
