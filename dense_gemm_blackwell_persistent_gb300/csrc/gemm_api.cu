@@ -329,7 +329,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     int dyn_units = 0, dyn_waves = 0;
     bool dyn = dynamic_lists(plan, p.num_tiles, resident, &dyn_units, &dyn_waves);
     // one cluster per list: keep the grid within the launch limit (x < 2^31), else stay static
-    if (dyn && ((int64_t)dyn_units + (p.num_tiles - (int64_t)dyn_units * dyn_waves)) * cluster >= (int64_t(1) << 31))
+    if (dyn && (int64_t)dyn_list_count(p.num_tiles, dyn_units, dyn_waves) * cluster >= (int64_t(1) << 31))
         dyn = false;
     const bool sk = !dyn && plan->stream_k && plan->d_partials != nullptr && plan->d_flags != nullptr;
     p.sched = make_schedule(p.num_tiles, resident, p.k_blocks, sk);
@@ -368,7 +368,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     if (rc != GEMM_OK) return rc;
 
     // clusters launched: the static schedule's units, or one per dynamic list
-    const int units = dyn ? dyn_units + (p.num_tiles - dyn_units * dyn_waves) : p.sched.units;
+    const int units = dyn ? dyn_list_count(p.num_tiles, dyn_units, dyn_waves) : p.sched.units;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * cluster), 1, 1);

@@ -419,10 +419,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // requested after a request that failed.
     const bool dyn = p.dynamic != 0;
     const int nwork = dyn ? 0 : work_count(p.sched, pair_id);
-    auto list_len = [&](int c) { return c < p.dyn_units ? p.dyn_waves : 1; };
-    auto list_tile = [&](int c, int k) {
-        return c < p.dyn_units ? c + k * p.dyn_units : p.dyn_units * p.dyn_waves + (c - p.dyn_units);
-    };
+    auto list_len = [&](int c) { return dyn_list_len(c, p.dyn_units, p.dyn_waves); };
+    auto list_tile = [&](int c, int k) { return dyn_list_tile(c, k, p.dyn_units, p.dyn_waves); };
     // Position in this unit's work: whose list, the next item in it, its
     // length, the next response to read.
     struct Cursor {

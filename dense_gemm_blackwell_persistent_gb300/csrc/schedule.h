@@ -161,4 +161,17 @@ GB300_HD Work work_item(const Schedule& s, int u, int j) {
     return w;
 }
 
+// Dynamic work list (cluster launch control): the grid has one cluster per
+// list of tiles.  Cluster c < units owns the whole tiles c, c + units, ...,
+// c + (waves - 1)·units of the persistent waves; cluster c >= units owns
+// the single tile units·waves + (c - units).  A running unit does its own
+// list, then the lists of clusters the hardware cancels for it, so every
+// tile runs exactly once whichever clusters start.  units = tiles, waves = 1
+// makes every tile a list of its own.
+GB300_HD int dyn_list_count(int tiles, int units, int waves) { return units + (tiles - units * waves); }
+GB300_HD int dyn_list_len(int c, int units, int waves) { return c < units ? waves : 1; }
+GB300_HD int dyn_list_tile(int c, int k, int units, int waves) {
+    return c < units ? c + k * units : units * waves + (c - units);
+}
+
 }  // namespace gb300

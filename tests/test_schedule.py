@@ -9,7 +9,9 @@ evenly, and the invariants the epilogue's fix-up relies on: a tile has at
 most two pieces; the piece with the tile's first k-blocks is its unit's last
 work item and finishes the tile; the other is its unit's first stream-K
 item; both name the same workspace slot (the second piece's unit) and the
-same flag; no slot or flag is used twice in a launch.
+same flag; no slot or flag is used twice in a launch.  For the dynamic work
+list (cluster launch control) they check that the clusters' lists cover
+every tile exactly once.
 """
 import os
 import subprocess
@@ -149,3 +151,60 @@ def test_random_shapes(dump):
         cases.append((T, P, KB, bool(rng.integers(0, 4) > 0)))
     for case, res in zip(cases, dump(cases)):
         check(res, *case)
+
+
+@pytest.fixture(scope="module")
+def dump_raw(tmp_path_factory):
+    exe = str(tmp_path_factory.mktemp("sched_dyn") / "schedule_dump")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, SRC, "-o", exe], check=True)
+
+    def run(cases):
+        inp = "".join(f"{t} {u} {w} -1\n" for t, u, w in cases)
+        out = subprocess.run([exe], input=inp, capture_output=True, text=True, check=True).stdout
+        results, cur = [], None
+        for line in out.splitlines():
+            f = line.split()
+            if f[0] == "D":
+                cur = {"head": tuple(map(int, f[1:])), "lists": defaultdict(list)}
+            elif f[0] == "L":
+                c, k, tile = map(int, f[1:])
+                assert k == len(cur["lists"][c])
+                cur["lists"][c].append(tile)
+            elif f[0] == "E":
+                results.append(cur)
+        return results
+    return run
+
+
+def dynamic_cases():
+    """(tiles, units, waves) as the host builds them: the partial last wave
+    handed out (units = resident units, waves = tiles // units, tiles not a
+    multiple), and every tile a list (units = tiles, waves = 1)."""
+    cases = []
+    for T in (77, 112, 304 + 5, 1024, 1184, 512, 6, 1):
+        for P in (76, 36, 152, 5):
+            if T > P and T % P:
+                cases.append((T, P, T // P))
+        cases.append((T, T, 1))
+    return cases
+
+
+def test_dynamic_lists_cover_every_tile_once(dump_raw):
+    """Every tile belongs to exactly one cluster's list, the persistent
+    clusters own the static raster's whole waves (c, c + P, ...), and each
+    tile of the partial wave is a list of its own."""
+    cases = dynamic_cases()
+    for (T, P, D), res in zip(cases, dump_raw(cases)):
+        t, u, w, n = res["head"]
+        assert (t, u, w) == (T, P, D) and n == P + (T - P * D)
+        owner = {}
+        for c in range(n):
+            lst = res["lists"][c]
+            if c < P:
+                assert lst == [c + k * P for k in range(D)], (T, P, D, c)
+            else:
+                assert lst == [P * D + (c - P)], (T, P, D, c)
+            for tile in lst:
+                assert tile not in owner, (T, P, D, tile)
+                owner[tile] = c
+        assert sorted(owner) == list(range(T)), (T, P, D)
