@@ -143,9 +143,9 @@ struct gemm_plan {
     void* hbuf[3] = {nullptr, nullptr, nullptr};
     size_t hcap[3] = {0, 0, 0};
     // gemm_plan_run_host's pipeline (created on first use): streams for the
-    // copies of B and of A, for the products and for the copies of C back;
+    // copies in (B, then A), for the products and for the copies of C back;
     // events: start, B resident, and per row chunk A resident / C computed.
-    cudaStream_t hstream[4] = {nullptr, nullptr, nullptr, nullptr};
+    cudaStream_t hstream[3] = {nullptr, nullptr, nullptr};
     cudaEvent_t hev_start = nullptr, hev_b = nullptr, hev_done = nullptr;
     cudaEvent_t hev_a[8] = {}, hev_c[8] = {};
 };
@@ -616,7 +616,7 @@ int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
 bool host_pipeline_ready(gemm_plan* plan) {
     if (plan->hstream[0]) return true;
     bool ok = true;
-    for (int i = 0; i < 4 && ok; ++i) ok = cudaStreamCreateWithFlags(&plan->hstream[i], cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 3 && ok; ++i) ok = cudaStreamCreateWithFlags(&plan->hstream[i], cudaStreamNonBlocking) == cudaSuccess;
     cudaEvent_t* evs[3] = {&plan->hev_start, &plan->hev_b, &plan->hev_done};
     for (int i = 0; i < 3 && ok; ++i) ok = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; i < 8 && ok; ++i)
@@ -624,9 +624,9 @@ bool host_pipeline_ready(gemm_plan* plan) {
              cudaEventCreateWithFlags(&plan->hev_c[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 3; ++i)
             if (plan->hstream[i]) cudaStreamDestroy(plan->hstream[i]);
-        for (int i = 0; i < 4; ++i) plan->hstream[i] = nullptr;
+        for (int i = 0; i < 3; ++i) plan->hstream[i] = nullptr;
     }
     return ok;
 }
@@ -656,25 +656,28 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
         }
     }
     if (!host_pipeline_ready(plan)) return GEMM_ERR_CUDA;
-    // The pipeline: B on one copy stream, A in row chunks on another; the
-    // product of each chunk starts as soon as its rows and B are resident,
-    // and its rows of C go back on a third stream while later chunks are
-    // computed.  Chunks are whole 256-row tiles (a CTA pair's tile height).
-    // One chunk per 1024 rows, at most 8: smaller chunks shorten the tail (the
-    // last chunk's product and copy back), but below ~1024 rows a chunk's
-    // product no longer fills a wave of tiles.  Measured on GB300 (host link
-    // ~209 GB/s in, ~192 GB/s out): 4096³ bf16 299 TFLOP/s end to end with 4
-    // chunks (290 with 8, 234 unpipelined), 8192³ 670 with 8 (428 unpipelined).
+    // The pipeline: B, then A in row chunks, on one copy stream (every
+    // chunk's product needs all of B, so B goes first); the product of each
+    // chunk starts as soon as its rows are resident, and its rows of C go
+    // back on another stream while later chunks are copied and computed.
+    // Chunks are whole 256-row tiles (a CTA pair's tile height).  One chunk
+    // per 1024 rows, at most 8: smaller chunks shorten the tail (the last
+    // chunk's product and copy back), but below ~1024 rows a chunk's product
+    // no longer fills a wave of tiles.  The host link bounds it: measured on
+    // GB300 ~208 GB/s in and ~192 GB/s out one way at a time, ~165 GB/s each
+    // way at once, the same whether the copy engines or SM loads and stores
+    // move the bytes; 4096³ bf16 runs at ~300 TFLOP/s end to end (234
+    // unpipelined), 8192³ at ~675.
     const int64_t want = std::max<int64_t>(1, std::min<int64_t>(8, M / 1024));
     int64_t rows = ((M + want - 1) / want + 255) / 256 * 256;
     const int nch = (int)((M + rows - 1) / rows);
     const size_t a_row_bytes = (size_t)K * elem_bytes(dtype), c_row_bytes = (size_t)N * elem_bytes(out_dtype);
-    cudaStream_t sB = plan->hstream[0], sA = plan->hstream[1], sX = plan->hstream[2], sC = plan->hstream[3];
+    cudaStream_t sA = plan->hstream[0], sX = plan->hstream[1], sC = plan->hstream[2];   // copies in, products, copies out
     bool ok = cudaEventRecord(plan->hev_start, s) == cudaSuccess;   // after the caller's earlier work
-    for (int i = 0; i < 4 && ok; ++i) ok = cudaStreamWaitEvent(plan->hstream[i], plan->hev_start, 0) == cudaSuccess;
+    for (int i = 0; i < 3 && ok; ++i) ok = cudaStreamWaitEvent(plan->hstream[i], plan->hev_start, 0) == cudaSuccess;
     if (ok && K > 0)
-        ok = cudaMemcpyAsync(plan->hbuf[1], B_host, bytes[1], cudaMemcpyHostToDevice, sB) == cudaSuccess &&
-             cudaEventRecord(plan->hev_b, sB) == cudaSuccess && cudaStreamWaitEvent(sX, plan->hev_b, 0) == cudaSuccess;
+        ok = cudaMemcpyAsync(plan->hbuf[1], B_host, bytes[1], cudaMemcpyHostToDevice, sA) == cudaSuccess &&
+             cudaEventRecord(plan->hev_b, sA) == cudaSuccess && cudaStreamWaitEvent(sX, plan->hev_b, 0) == cudaSuccess;
     for (int c = 0; c < nch && ok; ++c) {
         const int64_t r0 = c * rows, mc = std::min(rows, M - r0);
         const char* a_src = static_cast<const char*>(A_host) + (size_t)r0 * a_row_bytes;
@@ -778,7 +781,7 @@ int gemm_plan_destroy(gemm_plan_t plan) {
     if (plan->d_trace) cudaFree(plan->d_trace);
     for (int i = 0; i < 3; ++i)
         if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 3; ++i)
         if (plan->hstream[i]) cudaStreamDestroy(plan->hstream[i]);
     cudaEvent_t evs[3] = {plan->hev_start, plan->hev_b, plan->hev_done};
     for (cudaEvent_t e : evs)
