@@ -71,10 +71,11 @@ int get_encoder(EncodeTiledFn* out) {
 // A batch of row-major matrices rows×cols (cols contiguous), `count`
 // matrices `stride` elements apart, as a 3-D tensor map (cols, rows, batch);
 // box = box_rows × box_cols of one matrix; zero fill outside the tensor.  A
-// single matrix gets batch extent 1.
+// single matrix gets batch extent 1.  `fake_reject` (tests of the error
+// path) replaces the driver's encoder by one that rejects the map.
 int encode_3d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint64_t count,
               uint64_t stride, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle,
-              CUtensorMapL2promotion promo) {
+              CUtensorMapL2promotion promo, bool fake_reject = false) {
     EncodeTiledFn enc;
     int rc = get_encoder(&enc);
     if (rc != GEMM_OK) return rc;
@@ -84,8 +85,9 @@ int encode_3d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t
     cuuint64_t strides[2] = {cols * eb, stride * eb};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, tma_dtype(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fake_reject ? CUDA_ERROR_INVALID_VALUE
+                             : enc(map, tma_dtype(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }
 
@@ -130,6 +132,7 @@ struct gemm_plan {
     int dynamic = -1;             // run-time tile hand-out: 0 off, 1 the partial last wave, 2 every tile, -1 auto
     int64_t wait_limit_us = 0;    // bound on a kernel wait (0 = kWaitLimitNs)
     int stall_test = 0;           // tests of the timeout path only
+    int fail_encode = 0;          // tests of the error path only: the encoder rejects every map
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
@@ -364,7 +367,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     if (rc == GEMM_OK)
         rc = encode_3d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, (uint64_t)batch.count, (uint64_t)batch.sc, 32,
                        kChunkCols, out_dtype == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                       CU_TENSOR_MAP_L2_PROMOTION_NONE);
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE, plan->fail_encode != 0);
     if (rc != GEMM_OK) return rc;
 
     // clusters launched: the static schedule's units, or one per dynamic list
@@ -538,6 +541,10 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
         case GEMM_OPT_DYNAMIC:
             if (value < -1 || value > 2) return GEMM_ERR_INVALID_ARG;
             plan->dynamic = (int)value;
+            return GEMM_OK;
+        case GEMM_OPT_FAIL_ENCODE:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            plan->fail_encode = (int)value;
             return GEMM_OK;
         case GEMM_OPT_TILE_N: {
             if (value == 0) {

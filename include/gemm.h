@@ -117,7 +117,7 @@ typedef enum {
                                     run ends, after about two wait bounds, with
                                     GEMM_ERR_TIMEOUT (role 8) in the status word and
                                     C unwritten; 0 (default) = off                     */
-    GEMM_OPT_DYNAMIC = 9         /* run-time tile scheduling through cluster launch
+    GEMM_OPT_DYNAMIC = 9,        /* run-time tile scheduling through cluster launch
                                     control ("Writing Mosaic GPU kernels with Pallas",
                                     "Cluster launch control"): the grid gets one
                                     cluster per list of tiles, and a unit that has
@@ -133,6 +133,11 @@ typedef enum {
                                     of tiles on (where it measured faster), else 0;
                                     0 on plans with GEMM_OPT_MAX_CTAS or
                                     GEMM_OPT_STREAM_K set                          */
+    GEMM_OPT_FAIL_ENCODE = 10    /* tests of the error path only: 1 = the driver's
+                                    tensor-map encoder is replaced by a fake that
+                                    rejects the output map, so runs on this plan
+                                    return GEMM_ERR_DRIVER before any launch and
+                                    leave C untouched; 0 (default) = off            */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan

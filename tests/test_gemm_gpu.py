@@ -847,6 +847,32 @@ def test_bounded_wait_expires_and_plan_recovers(g, fresh_plan, unit, dynamic):
     assert np.array_equal(C, C_ref)
 
 
+def test_encoder_failure_is_reported_before_any_launch(g, fresh_plan):
+    """Failure detection on the host: with the test option on, the driver's
+    tensor-map encoder is replaced by a fake that rejects the map.  The run
+    must return GEMM_ERR_DRIVER, launch nothing (C keeps its NaN poison, the
+    last launch record is unchanged, the device status is clean), and the
+    same plan must compute correctly once the option is off."""
+    M, N, K = 300, 264, 136
+    A, B = draw(M, N, K, dist="int", seed=61)
+    Ad, Bd = A.cuda(), B.cuda()
+    run(g, fresh_plan, Ad, Bd, wl.F32)
+    before = g.gemm_plan_last_launch(fresh_plan)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_FAIL_ENCODE, 1)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                        torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == g.GEMM_ERR_DRIVER
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(C).all()), "a rejected run wrote C"
+    assert g.gemm_plan_last_launch(fresh_plan) == before
+    assert g.gemm_plan_status(fresh_plan) == g.GEMM_OK
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_FAIL_ENCODE, 0)
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32)), C_ref)
+
+
 def test_wait_options_are_checked(g, fresh_plan):
     import ctypes
     p = ctypes.c_void_p(fresh_plan)
