@@ -208,16 +208,35 @@ def _dtype_code(t) -> int:
     return codes[t]
 
 
+_default_plans = {}
+
+
+def default_plan(device=None) -> int:
+    """A plan for `device` (torch device or index; default: the current one),
+    created on first use and kept for the life of the process; what
+    matmul() and bmm() use when no plan is passed."""
+    import torch
+    if device is None:
+        idx = torch.cuda.current_device()
+    else:
+        d = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        idx = d.index if d.index is not None else torch.cuda.current_device()
+    if idx not in _default_plans:
+        _default_plans[idx] = gemm_plan_create(idx)
+    return _default_plans[idx]
+
+
 def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: bool = False,
            b_kn: bool = False):
     """C = A @ B.T for CUDA tensors A [M,K], B [N,K] (contiguous; bf16, f16,
     float8_e4m3fn or float8_e5m2, both the same).
 
     a_km / b_kn: A is given as [K,M] / B as [K,N] (both contiguous), read in
-    place by the tensor cores (16-bit inputs; needs a plan), so
-    ``matmul(A, B, b_kn=True)`` is the plain A @ B.
+    place by the tensor cores (16-bit inputs), so ``matmul(A, B, b_kn=True)``
+    is the plain A @ B.
     out_dtype: torch.float32, torch.bfloat16 or torch.float16 (default: A's
     dtype for 16-bit inputs, bf16 for fp8 inputs).
+    plan: default_plan(A.device) when omitted.
     Runs on torch's current stream of A's device.
     """
     import torch
@@ -243,24 +262,25 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: boo
     elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M,N] tensor of out_dtype")
     stream = torch.cuda.current_stream(A.device).cuda_stream
+    if plan is None:
+        plan = default_plan(A.device)
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, _dtype_code(A.dtype),
             _dtype_code(out_dtype), stream)
     if layout:
-        if plan is None:
-            raise ValueError("a_km / b_kn need an explicit plan (gemm_plan_run_layout)")
         gemm_plan_run_layout(plan, *args[:-1], layout, args[-1])
-    elif plan is None:
-        gemm_run(*args)
     else:
         gemm_plan_run(plan, *args)
     return out
 
 
-def bmm(A, B, plan: int, out_dtype=None, out=None):
+def bmm(A, B, plan: Optional[int] = None, out_dtype=None, out=None):
     """C[e] = A[e] @ B[e].T for CUDA tensors A [batch,M,K] or [M,K] (shared) and
     B [batch,N,K] or [N,K] (shared), contiguous, same 16-bit or 8-bit dtype,
-    in one launch (gemm_plan_run_batched).  Returns C [batch,M,N]."""
+    in one launch (gemm_plan_run_batched; plan: default_plan(A.device) when
+    omitted).  Returns C [batch,M,N]."""
     import torch
+    if plan is None:
+        plan = default_plan(A.device)
     if A.dim() not in (2, 3) or B.dim() not in (2, 3) or A.shape[-1] != B.shape[-1]:
         raise ValueError("A must be [batch,M,K] or [M,K], B [batch,N,K] or [N,K]")
     if A.dtype != B.dtype or not (A.is_contiguous() and B.is_contiguous()):

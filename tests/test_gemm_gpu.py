@@ -931,6 +931,20 @@ def test_deterministic(g, plan):
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
 
 
+def test_helpers_without_a_plan(g):
+    """matmul() and bmm() without a plan use one default plan per device,
+    created on first use and reused."""
+    A, B = draw(264, 200, 136, dist="int", seed=71)
+    C = g.matmul(A.cuda(), B.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    C_ref, _ = oracle_full(A, B)
+    assert np.array_equal(parity.to_f64(C), C_ref)
+    assert g.default_plan() == g.default_plan(0) == g.default_plan(torch.device("cuda", 0))
+    C3 = g.bmm(A.cuda().view(1, 264, 136), B.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.to_f64(C3[0]), C_ref)
+
+
 def test_torch_matmul_helper(g, plan):
     A, B = draw(256, 512, 128, seed=3)
     Ad, Bd = A.cuda(), B.cuda()
