@@ -774,8 +774,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (w.ncontrib == 1 && gn == 0) {
                 // The unit's last tile: nothing overlaps its epilogue, and its
                 // operand ring is idle (no later loads, every MMA done), so each
-                // chunk gets its own box there, one fence covers them all and
-                // the stores go out back to back.
+                // chunk gets its own box there: no chunk waits for an earlier
+                // store to finish reading, and each is stored as soon as it is
+                // staged.
                 if (row0 < p.M) {
                     const uint32_t region = base + (uint32_t)(warp - 2) * (uint32_t)(kChunks * C::kSlotBytes);
                     uint32_t ra[32], rb[32];
@@ -787,15 +788,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
                         if (c + 1 < kChunks) tmem_ld_32x32b_x32(t_row + (c + 1) * kChunkCols, nxt);
                         stage_chunk(region + (uint32_t)(c * C::kSlotBytes), cur);
+                        fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0 && col0 + c * kChunkCols < p.N)
+                            tma_store_3d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0, bt);
                         if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
-                    fence_proxy_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        for (int c = 0; c < kChunks && col0 + c * kChunkCols < p.N; ++c)
-                            tma_store_3d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0, bt);
-                        bulk_commit_group();
-                    }
+                    if (lane == 0) bulk_commit_group();
                 }
             } else if (w.ncontrib == 1) {
                 if (row0 < p.M) {
