@@ -384,6 +384,54 @@ def test_dynamic_schedule_in_cuda_graph(g, fresh_plan, mode):
         assert np.array_equal(parity.to_f64(Cd), C_ref), f"replay with seed {seed}"
 
 
+def test_many_launches_mixed_schedules(g):
+    """Back-to-back launches cycling through every schedule (static, stream-K,
+    dynamic work lists) and unit size on two streams at once, each plan kept
+    on one stream: every result stays exact.  Catches state that leaks from
+    one launch into the next (stream-K flags, response rings, accumulators)."""
+    shapes = [(2048, 4096, 64), (1300, 1096, 520), (768, 3072, 264)]
+    data = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = draw(M, N, K, dist="int", seed=900 + i)
+        C_ref, _ = oracle_full(A, B)
+        data.append((M, N, K, A.cuda(), B.cuda(), torch.from_numpy(C_ref)))
+    configs = [(d, sk, u) for d in (0, 1, 2) for sk in (0, 1) for u in UNITS]
+    plans = []
+    for d, sk, u in configs:
+        p = g.gemm_plan_create(0)
+        configure(g, p, u)
+        g.gemm_plan_set_option(p, g.GEMM_OPT_DYNAMIC, d)
+        g.gemm_plan_set_option(p, g.GEMM_OPT_STREAM_K, sk)
+        plans.append(p)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    try:
+        pending = []
+        for it in range(20 * len(configs)):
+            si, ci = it % len(shapes), (it // len(shapes)) % len(configs)
+            M, N, K, Ad, Bd, _ = data[si]
+            st = streams[ci % 2]
+            C = torch.full((M, N), float("nan"), device="cuda")
+            with torch.cuda.stream(st):
+                g.gemm_plan_run(plans[ci], Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                                st.cuda_stream)
+            pending.append((it, C, si))
+            if len(pending) == 24:
+                torch.cuda.synchronize()
+                for j, Cj, sj in pending:
+                    cfg = configs[(j // len(shapes)) % len(configs)]
+                    assert torch.equal(Cj.cpu().double(), data[sj][5]), f"launch {j}: {shapes[sj]} {cfg}"
+                pending.clear()
+        torch.cuda.synchronize()
+        for j, Cj, sj in pending:
+            assert torch.equal(Cj.cpu().double(), data[sj][5]), f"launch {j}"
+        for p in plans:
+            assert g.gemm_plan_status(p) == 0
+    finally:
+        torch.cuda.synchronize()
+        for p in plans:
+            g.gemm_plan_destroy(p)
+
+
 def test_dynamic_and_static_agree(g, fresh_plan):
     """The schedule decides only where a tile is computed, not how: the
     same inputs give bitwise the same C every way."""
