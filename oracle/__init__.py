@@ -1,7 +1,8 @@
 """CPU oracle for C = A·Bᵀ (fp64), with its build step.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
-benchmark's CPU-baseline leg are the only callers.  The library's product path
+benchmark's CPU-baseline leg and reference arm (``--impl reference``) are the
+only callers.  The library's product path
 never imports this package, and this package imports nothing from the library.
 
 The arithmetic lives in ``gemm_oracle.c`` (plain C, fp64 triple loop,

@@ -3,7 +3,7 @@
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may link,
  * load or call this file; only the tests, the package's smoke check and the
- * benchmark's CPU-baseline leg use it.  It shares no code, header or table
+ * benchmark's CPU-baseline leg and reference arm (--impl reference) use it.  It shares no code, header or table
  * with the CUDA path: it decodes the 16-bit input formats itself and sums in
  * double precision in the plainest order.
  *
