@@ -112,7 +112,10 @@ def gemm_run(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int, out_dty
 def gemm_run_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int, out_dtype: int,
                      stream: int = 0) -> None:
     """Allocation-free gemm_run: for callers that may not allocate device memory
-    (inside CUDA-graph capture, fixed memory pools, foreign allocators)."""
+    (services whose pool owns all of HBM, embedders under a foreign allocator,
+    loops that cannot take a cudaFree's device-wide synchronisation).  The
+    first call on a device sets that device up; make it before any stream
+    capture.  Calls that overlap on the GPU share one status record and race."""
     _check(_lib.gemm_run_noalloc(_vp(A), _vp(B), _vp(C), M, N, K, dtype, out_dtype, _vp(stream)),
            "gemm_run_noalloc")
 

@@ -831,12 +831,11 @@ const char* gemm_strerror(int status) {
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.
 //
-// Some callers may not allocate device memory at all: code that runs while a
-// stream is being captured into a CUDA graph (cudaMalloc is not a stream
-// operation and breaks or invalidates the capture), services that reserve
+// Some callers may not allocate device memory at all: services that reserve
 // every byte of HBM for their own pool at start-up and forbid allocations
-// afterwards, and embedders whose memory is owned by another allocator that
-// must see every device allocation.  gemm_plan_create() allocates the plan's
+// afterwards, embedders whose memory is owned by another allocator that must
+// see every device allocation, and latency-critical loops that cannot take
+// the device-wide synchronisation a cudaFree implies.  gemm_plan_create() allocates the plan's
 // 16-byte status record with cudaMalloc, so those callers use
 // gemm_run_noalloc() instead.  It launches the same kernel, but the kernel's
 // only scratch -- the status record its bounded waits write on timeout --

@@ -232,10 +232,12 @@ int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* 
 int gemm_plan_destroy(gemm_plan_t plan);
 
 /* Allocation-free form of gemm_run(), for callers that may not allocate
- * device memory at all: code running while a stream is being captured into
- * a CUDA graph, services that hand all of HBM to their own pool at start-up
- * and forbid later allocations, embedders whose memory belongs to another
- * allocator.  No plan is needed and nothing is allocated, now or later (no
+ * device memory at all: services that hand all of HBM to their own pool at
+ * start-up and forbid later allocations (a cudaMalloc would fail or carve
+ * into memory the pool counts as its own), embedders whose device memory
+ * belongs to another allocator that must account for every byte, and
+ * latency-critical loops that cannot afford the device-wide synchronisation
+ * a cudaFree implies.  No plan is needed and nothing is allocated, now or later (no
  * cudaMalloc, no cudaFree, no allocating library call): the kernel's only
  * scratch, its 16-byte status record, lives in a 256-byte static device
  * array that every GPU loading this library keeps until the process exits.

