@@ -126,10 +126,17 @@ def main():
     gemm_plan_trace(plan)
     if not a.no_flush:
         torch.empty(512 << 20, dtype=torch.uint8, device="cuda").zero_()   # evict A, B, C from L2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
     gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), a.M, a.N, a.K, a.dtype, a.out, s)
+    e1.record()
     torch.cuda.synchronize()
     buf = gemm_plan_trace(plan)
     res = summarise(buf, gemm_plan_last_grid(plan))
+    # The launch as CUDA events see it, beside the span the CTAs themselves
+    # stamped (first entry to last exit): the difference is launch and
+    # completion latency outside the kernel's code.
+    res["event_us"] = round(e0.elapsed_time(e1) * 1e3, 2)
     launch = gemm_plan_last_launch(plan)
     print(f"{a.M}x{a.N}x{a.K} unit={launch['ctas_per_unit']} tile_n={launch['tile_n']} ctas={launch['ctas']} "
           f"stream_k={a.stream_k} l2={'warm' if a.no_flush else 'flushed'}: "

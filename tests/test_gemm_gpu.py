@@ -779,6 +779,25 @@ def test_medium_ragged_full(g, plan):
     parity.assert_within(C, C_ref, S, w.out_dtype, "ragged 1000x760x1256")
 
 
+def test_output_beyond_2_pow_32_elements(g, plan):
+    """A C of more than 2^32 elements (66000 × 65600, bf16, 8.7 GB), ragged
+    against every tile width, in the default launch: no 32-bit offset wraps
+    anywhere between the host's tensor maps and the last tile's stores.
+    Every element is written (C is NaN-poisoned and checked in row blocks);
+    sampled entries, the corners and the tile edges match the oracle."""
+    M, N, K = 66000, 65600, 64
+    assert M * N > 1 << 32
+    A, B = draw(M, N, K, seed=41)
+    C = run(g, plan, A.cuda(), B.cuda(), wl.BF16)
+    for r in range(0, M, 8192):
+        assert bool(torch.isfinite(C[r:r + 8192]).all()), f"unwritten or non-finite entries in rows {r}.."
+    I, J = parity.sample_positions(M, N, 2048, seed=41, tile_m=4096, tile_n=4096)
+    got = C[torch.from_numpy(I).cuda(), torch.from_numpy(J).cuda()].to("cpu", torch.float64).numpy()
+    del C
+    C_ref, S = oracle.gemm_entries(wl.as_bits(A), wl.as_bits(B), wl.BF16, I, J)
+    parity.assert_within(got, C_ref, S, wl.BF16, f"{M}x{N}x{K}")
+
+
 # ------------------------------------------------------------------ edges and API behaviour
 
 @pytest.mark.parametrize("unit", UNITS)
