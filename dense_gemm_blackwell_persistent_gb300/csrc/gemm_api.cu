@@ -137,6 +137,9 @@ struct gemm_plan {
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
     int* d_status = nullptr;      // 4 ints, see Params::status
+    // The last run's launch shape, for reports.  Every run writes it, so
+    // runs from several host threads at once take rec_mu for it.
+    std::mutex rec_mu;
     int last_grid = 0;
     int last_tile_n = 0;
     int last_unit = 0;
@@ -399,6 +402,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
+    std::lock_guard<std::mutex> lk(plan->rec_mu);
     plan->last_grid = units * cluster;
     plan->last_tile_n = bn;
     plan->last_unit = cluster;
@@ -742,6 +746,7 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status) {
 
 int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
     if (!plan || !ctas) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(plan->rec_mu);
     *ctas = plan->last_grid;
     return GEMM_OK;
 }
@@ -749,6 +754,7 @@ int gemm_plan_last_grid(gemm_plan_t plan, int* ctas) {
 int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* tile_n, int* dp_waves,
                           int* sk_tiles) {
     if (!plan || !ctas || !ctas_per_unit || !tile_n || !dp_waves || !sk_tiles) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(plan->rec_mu);
     *ctas = plan->last_grid;
     *ctas_per_unit = plan->last_unit;
     *tile_n = plan->last_tile_n;
@@ -759,6 +765,7 @@ int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* 
 
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
     if (!plan || !tile_n) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(plan->rec_mu);
     *tile_n = plan->last_tile_n;
     return GEMM_OK;
 }

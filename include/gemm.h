@@ -37,9 +37,11 @@
  *
  * Threads.  A plan may be used from several host threads and streams at
  * once; calls build their tensor maps on the host stack and share only
- * read-only plan state plus the device status word.  Exception: with the
- * stream-K option on (off by default) runs share the plan's workspace, so
- * runs that may overlap on the GPU must then use different plans.
+ * read-only plan state, the device status word and the last-launch record
+ * (written under a lock by every run; with concurrent runs it describes one
+ * of them).  Exception: with the stream-K option on (off by default) runs
+ * share the plan's workspace, so runs that may overlap on the GPU must then
+ * use different plans.
  */
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H

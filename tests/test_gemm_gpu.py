@@ -432,6 +432,57 @@ def test_many_launches_mixed_schedules(g):
             g.gemm_plan_destroy(p)
 
 
+def test_host_threads_share_one_plan(g, fresh_plan):
+    """Four host threads, each on a stream of its own, run products of their
+    own shapes through one plan at the same time (the C calls release the
+    GIL, so the library's host code runs concurrently too): every result is
+    exact, the last-launch record stays readable throughout, and the plan's
+    device status stays clean."""
+    import threading
+    shapes = [(1300, 1096, 520), (768, 3072, 264), (2048, 1024, 136), (520, 776, 1032)]
+    data = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = draw(M, N, K, dist="int", seed=950 + i)
+        C_ref, _ = oracle_full(A, B)
+        data.append((A.cuda(), B.cuda(), torch.from_numpy(C_ref)))
+    torch.cuda.synchronize()
+    errors = []
+    start = threading.Barrier(len(shapes))
+
+    def worker(t):
+        try:
+            torch.cuda.set_device(0)
+            M, N, K = shapes[t]
+            Ad, Bd, C_ref = data[t]
+            st = torch.cuda.Stream()
+            outs = []
+            start.wait()
+            with torch.cuda.stream(st):
+                for _ in range(30):
+                    C = torch.full((M, N), float("nan"), device="cuda")
+                    g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, wl.BF16,
+                                    wl.F32, st.cuda_stream)
+                    launch = g.gemm_plan_last_launch(fresh_plan)
+                    assert launch["ctas_per_unit"] in (1, 2, 4) and launch["ctas"] > 0, launch
+                    outs.append(C)
+            st.synchronize()
+            for j, C in enumerate(outs):
+                if not torch.equal(C.cpu().double(), C_ref):
+                    errors.append(f"thread {t}, launch {j}: {shapes[t]} not exact")
+                    break
+        except Exception as e:   # reported below: an exception in a thread would be lost
+            errors.append(f"thread {t}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(len(shapes))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert g.gemm_plan_status(fresh_plan) == 0
+
+
 def test_dynamic_and_static_agree(g, fresh_plan):
     """The schedule decides only where a tile is computed, not how: the
     same inputs give bitwise the same C every way."""
