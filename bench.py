@@ -364,19 +364,23 @@ def main():
         try:
             for _ in range(5):
                 ref_call()
-            cs, ce = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            cms = []
-            for _ in range(50):
+            # Same protocol as the timed steps: events around each launch on
+            # the stream, no host synchronisation inside the loop (a host
+            # wait per run would put the next launch's host-side latency
+            # inside its events whenever no flush is queued ahead of it).
+            cs = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+            ce = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
+            for i in range(50):
                 if flush is not None:
                     flush.zero_()
-                cs.record(stream)
+                cs[i].record(stream)
                 ref_call()
-                ce.record(stream)
-                ce.synchronize()
-                cms.append(cs.elapsed_time(ce))
-            cm = statistics.mean(cms)
+                ce[i].record(stream)
+            torch.cuda.synchronize()
+            cm = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
+            l2 = "L2 flushed" if flush is not None else "L2 not flushed"
             extra["cublas_reference"] = {"value": w.flops / (cm / 1e3) / 1e12, "unit": "TFLOP/s", "ms": cm,
-                                         "how": f"{ref_how}, same inputs, same process, 50 runs, L2 flushed"}
+                                         "how": f"{ref_how}, same inputs, same process, 50 runs, {l2}"}
         except RuntimeError as e:   # a torch build without this fp8 path: no reference line
             extra["cublas_reference"] = {"unavailable": str(e).splitlines()[0][:200]}
 

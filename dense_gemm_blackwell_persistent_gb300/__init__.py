@@ -45,7 +45,7 @@ if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: {_REBUILD}")
 
 _lib = ctypes.CDLL(LIB_PATH)
-_missing = [n for n in ("gemm_plan_create", "gemm_plan_run_batched", "gemm_probe_mma_rate", "gemm_run_noalloc")
+_missing = [n for n in ("gemm_plan_create", "gemm_plan_run_batched", "gemm_probe_mma_rate_n", "gemm_run_noalloc")
             if not hasattr(_lib, n)]
 if _missing:
     raise ImportError(f"{LIB_PATH} is out of date (no {', '.join(_missing)}): {_REBUILD}")
@@ -69,12 +69,13 @@ _lib.gemm_plan_last_launch.argtypes = [_vp] + [ctypes.POINTER(_int)] * 5
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]
 _lib.gemm_probe_mma_rate.argtypes = [_int, _int, _i64] + [ctypes.POINTER(ctypes.c_double)] * 3
+_lib.gemm_probe_mma_rate_n.argtypes = [_int, _int, _int, _i64] + [ctypes.POINTER(ctypes.c_double)] * 3
 _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_run_batched", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
               "gemm_plan_last_launch",
-              "gemm_plan_trace", "gemm_plan_destroy", "gemm_probe_mma_rate"):
+              "gemm_plan_trace", "gemm_plan_destroy", "gemm_probe_mma_rate", "gemm_probe_mma_rate_n"):
     getattr(_lib, _name).restype = _int
 
 
@@ -120,12 +121,12 @@ def gemm_run_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, dtype: int,
            "gemm_run_noalloc")
 
 
-def gemm_probe_mma_rate(dtype: int = 0, cta_pair: int = 2, mmas_per_sm: int = 1 << 16) -> dict:
+def gemm_probe_mma_rate(dtype: int = 0, cta_pair: int = 2, mmas_per_sm: int = 1 << 16, tile_n: int = 256) -> dict:
     """Tensor-core issue-rate probe on the current device (see include/gemm.h):
-    back-to-back MMAs of the GEMM's shape on every SM, no loads."""
+    back-to-back MMAs of the GEMM's shape (N = tile_n) on every SM, no loads."""
     fpc, tf, mhz = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
-    _check(_lib.gemm_probe_mma_rate(int(dtype), int(cta_pair), int(mmas_per_sm), ctypes.byref(fpc),
-                                    ctypes.byref(tf), ctypes.byref(mhz)), "gemm_probe_mma_rate")
+    _check(_lib.gemm_probe_mma_rate_n(int(dtype), int(cta_pair), int(tile_n), int(mmas_per_sm), ctypes.byref(fpc),
+                                      ctypes.byref(tf), ctypes.byref(mhz)), "gemm_probe_mma_rate_n")
     return {"flop_per_clk_per_sm": fpc.value, "tflops": tf.value, "sm_mhz": mhz.value}
 
 

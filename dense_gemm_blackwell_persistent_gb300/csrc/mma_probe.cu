@@ -10,10 +10,10 @@
 // Mojo (Part 2)" (the kernels are measured against the tensor cores' peak),
 // taken on the GPU itself rather than from a data sheet.
 //
-// The instruction stream is the persistent GEMM's: 128×256×16 (bf16/f16,
-// kind::f16) or 128×256×32 (8-bit, kind::f8f6f4) per CTA and instruction,
+// The instruction stream is the persistent GEMM's: 128×N×16 (bf16/f16,
+// kind::f16) or 128×N×32 (8-bit, kind::f8f6f4) per CTA and instruction,
 // M = 256 across a pair, K-major 128-byte-swizzled operands, four
-// instructions per 128-byte k-block.
+// instructions per 128-byte k-block; N is 256 or any tile width asked for.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -185,9 +185,11 @@ int run_probe(int sm_count, int64_t k_blocks, uint32_t idesc, std::vector<unsign
     return rc;
 }
 
-uint32_t probe_idesc(int dtype, int pair) {
+// Instruction descriptor of the probe's MMA: n accumulator columns (the
+// instruction's N, the GEMM's tile width), M = 128 per CTA.
+uint32_t probe_idesc(int dtype, int pair, int n) {
     const uint32_t ab = (dtype == GEMM_BF16 || dtype == GEMM_E5M2) ? 1u : 0u;
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kProbeN >> 3) << 17) |
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)((kRowsPerCta * pair) >> 4) << 24);
 }
 
@@ -198,9 +200,17 @@ using namespace gb300;
 
 extern "C" int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm, double* flop_per_clk_per_sm,
                                    double* tflops, double* sm_mhz) {
+    return gemm_probe_mma_rate_n(dtype, cta_pair, kProbeN, mmas_per_sm, flop_per_clk_per_sm, tflops, sm_mhz);
+}
+
+extern "C" int gemm_probe_mma_rate_n(int dtype, int cta_pair, int tile_n, int64_t mmas_per_sm,
+                                     double* flop_per_clk_per_sm, double* tflops, double* sm_mhz) {
     if (dtype != GEMM_BF16 && dtype != GEMM_F16 && dtype != GEMM_E4M3 && dtype != GEMM_E5M2)
         return GEMM_ERR_INVALID_ARG;
     if (cta_pair != 1 && cta_pair != 2) return GEMM_ERR_INVALID_ARG;
+    // N of an M = 128 (one CTA) or M = 256 (pair) instruction: 16..256 in steps of 16;
+    // the operand and TMEM buffers are sized for 256.
+    if (tile_n < 16 || tile_n > kProbeN || tile_n % 16 != 0) return GEMM_ERR_INVALID_ARG;
     const int per_block = kBlockKBytes / kMmaKBytes;
     if (mmas_per_sm < per_block || mmas_per_sm > (int64_t(1) << 24) || mmas_per_sm % per_block != 0)
         return GEMM_ERR_INVALID_ARG;
@@ -212,7 +222,7 @@ extern "C" int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm,
     }
     if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_NO_DEVICE;
     const bool f8 = dtype == GEMM_E4M3 || dtype == GEMM_E5M2;
-    const uint32_t idesc = probe_idesc(dtype, cta_pair);
+    const uint32_t idesc = probe_idesc(dtype, cta_pair, tile_n);
     const int64_t k_blocks = mmas_per_sm / per_block;
     std::vector<unsigned long long> out;
     float ms = 0.f;
@@ -222,8 +232,8 @@ extern "C" int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm,
     else rc = f8 ? run_probe<1, true>(prop.multiProcessorCount, k_blocks, idesc, out, &ms)
                  : run_probe<1, false>(prop.multiProcessorCount, k_blocks, idesc, out, &ms);
     if (rc != GEMM_OK) return rc;
-    // per SM and instruction: 128 rows × 256 columns × K (16, or 32 for 8-bit) multiply-adds
-    const double flop_per_mma = 2.0 * kRowsPerCta * kProbeN * (f8 ? 32 : 16);
+    // per SM and instruction: 128 rows × tile_n columns × K (16, or 32 for 8-bit) multiply-adds
+    const double flop_per_mma = 2.0 * kRowsPerCta * tile_n * (f8 ? 32 : 16);
     std::vector<double> fpc, mhz;
     for (size_t c = 0; c + 1 < out.size(); c += 2) {
         if (out[c] == 0 || out[c + 1] == 0) continue;   // a pair's second CTA records nothing

@@ -278,6 +278,14 @@ int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N
 int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm, double* flop_per_clk_per_sm,
                         double* tflops, double* sm_mhz);
 
+/* The same probe with instructions of N = tile_n accumulator columns (a
+ * tile width of the GEMM: 16..256 in steps of 16) instead of 256, so that
+ * the tensor cores' own rate at a narrower tile can be told apart from the
+ * cost of feeding that tile.  FLOP counts use tile_n.  Errors as above;
+ * GEMM_ERR_INVALID_ARG for any other tile_n. */
+int gemm_probe_mma_rate_n(int dtype, int cta_pair, int tile_n, int64_t mmas_per_sm, double* flop_per_clk_per_sm,
+                          double* tflops, double* sm_mhz);
+
 const char* gemm_strerror(int status);
 
 #ifdef __cplusplus

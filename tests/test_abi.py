@@ -85,6 +85,8 @@ def test_host_validation_without_gpu(lib):
     assert rs("gemm_probe_mma_rate", 2, 2, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG   # fp32 operands
     assert rs("gemm_probe_mma_rate", 0, 4, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG   # 4 CTAs
     assert rs("gemm_probe_mma_rate", 0, 2, 6, None, None, None) == lib.GEMM_ERR_INVALID_ARG         # not whole k-blocks
+    for n in (0, 8, 100, 272):                                                                      # not an MMA width
+        assert rs("gemm_probe_mma_rate_n", 0, 2, n, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG
     for code in range(-8, 1):
         assert lib.gemm_strerror(code) != "unknown status"
 

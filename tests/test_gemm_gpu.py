@@ -517,11 +517,27 @@ def test_mma_probe_rate(g, dtype, nominal, pair):
     assert 0.8 < r["tflops"] / expect < 1.1, (r, expect)
 
 
+@pytest.mark.parametrize("tile_n", [256, 224, 192, 160, 128, 64])
+def test_mma_probe_rate_by_tile_width(g, tile_n):
+    """The tensor cores' own rate for a pair's 256×N instructions: the full
+    dense rate at every GEMM tile width from 128 to 256 (so a narrow tile
+    that runs slower per k-block than its MMA work is held up by feeding,
+    not by the MMA); N = 64 is below it (measured ~5660 FLOP/clk/SM)."""
+    r = g.gemm_probe_mma_rate(wl.BF16, 2, 1 << 15, tile_n=tile_n)
+    if tile_n >= 128:
+        assert abs(r["flop_per_clk_per_sm"] / 8192 - 1) < 0.02, r
+    else:
+        assert 0 < r["flop_per_clk_per_sm"] < 8192 * 1.02, r
+
+
 def test_mma_probe_arguments(g):
     import ctypes
     d = ctypes.c_double()
     for args in ((wl.F32, 2, 1 << 12), (wl.BF16, 3, 1 << 12), (wl.BF16, 2, 6), (wl.BF16, 2, 0), (wl.BF16, 2, 1 << 25)):
         assert g.raw_status("gemm_probe_mma_rate", *args, ctypes.byref(d), None, None) == g.GEMM_ERR_INVALID_ARG
+    for n in (0, 8, 100, 272):
+        assert g.raw_status("gemm_probe_mma_rate_n", wl.BF16, 2, n, 1 << 12, ctypes.byref(d), None, None) \
+            == g.GEMM_ERR_INVALID_ARG
 
 
 # ------------------------------------------------------------------ 8-bit float inputs
