@@ -110,11 +110,15 @@ uint32_t make_idesc(int in_dtype, int m, int n, int layout) {
            | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// C = 0 for K == 0 (the empty sum).  `n16` 16-byte words.
-__global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16) {
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
-        c[i] = make_uint4(0u, 0u, 0u, 0u);
+// C = 0 for K == 0 (the empty sum): `count` matrices of `n16` 16-byte words,
+// `stride16` words apart, in one launch.
+__global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16, int64_t count, size_t stride16) {
+    const size_t step = (size_t)gridDim.x * blockDim.x;
+    for (int64_t e = 0; e < count; ++e) {
+        uint4* m = c + (size_t)e * stride16;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += step)
+            m[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 }  // namespace
@@ -293,11 +297,12 @@ bool dynamic_lists(const gemm_plan* plan, int64_t tiles, int64_t resident, int* 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
            int out_dtype, cudaStream_t stream, int layout = 0, const Batch& batch = Batch()) {
     if (K == 0) {
+        // N·out_bytes and, for batches, the C stride in bytes are 16-byte multiples (checked by the callers)
         const size_t n16 = (size_t)M * (size_t)N * elem_bytes(out_dtype) / 16;
+        const size_t stride16 = batch.count > 1 ? (size_t)batch.sc * elem_bytes(out_dtype) / 16 : 0;
         const int blocks = (int)std::min<size_t>((n16 + 255) / 256, (size_t)plan->sm_count * 8);
-        for (int64_t e = 0; e < batch.count; ++e)
-            fill_zero_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(
-                reinterpret_cast<uint4*>(static_cast<char*>(C) + (size_t)(e * batch.sc) * elem_bytes(out_dtype)), n16);
+        fill_zero_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(reinterpret_cast<uint4*>(C), n16, batch.count,
+                                                                  stride16);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;

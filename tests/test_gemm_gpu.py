@@ -891,6 +891,21 @@ def test_k_zero_writes_zeros(g, plan):
         assert bool((C == 0).all())
 
 
+def test_k_zero_batched_writes_zeros_only_in_the_products(g, plan):
+    """K = 0 in a batch: every product is the empty sum, written in one
+    launch; the gap between strided outputs stays untouched."""
+    M, N, batch, sc = 37, 48, 3, 37 * 48 + 64
+    A = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    C = torch.full((batch * sc,), float("nan"), dtype=torch.float32, device="cuda")
+    g.gemm_plan_run_batched(plan, A.data_ptr(), A.data_ptr(), C.data_ptr(), batch, M, N, 0, 0, 0, sc, wl.BF16,
+                            wl.F32, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(plan) == 0
+    view = C.view(batch, sc)
+    assert bool((view[:, :M * N] == 0).all())
+    assert bool(torch.isnan(view[:, M * N:]).all())
+
+
 def test_m_or_n_zero_is_noop(g, plan):
     A = torch.randn(0, 64, device="cuda").to(torch.bfloat16)
     B = torch.randn(16, 64, device="cuda").to(torch.bfloat16)
