@@ -137,6 +137,7 @@ struct gemm_plan {
     int64_t wait_limit_us = 0;    // bound on a kernel wait (0 = kWaitLimitNs)
     int stall_test = 0;           // tests of the timeout path only
     int fail_encode = 0;          // tests of the error path only: the encoder rejects every map
+    int visible_devices = 1;      // GPUs the process sees (multicast only with one)
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
@@ -198,10 +199,14 @@ int max_resident_ctas(const gemm_plan* plan) {
 // 32-byte sector, the load path becomes the bound, and halving the B reads
 // wins (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of
 // all SMs wins (4-CTA clusters fit on 144 of the 152 SMs).
+// Multicast is used only while the process sees a single GPU (a process
+// that may drive several runs no multicast code at all); an explicit
+// request on a plan that sees more is refused in launch().
 int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype, int layout) {
     if (plan->pair != 2) return 1;
-    const bool mc = plan->multicast == 1 ||
-                    (plan->multicast < 0 && layout == 0 && (K * elem_bytes(in_dtype)) % 128 != 0);
+    const bool mc = plan->visible_devices == 1 &&
+                    (plan->multicast == 1 ||
+                     (plan->multicast < 0 && layout == 0 && (K * elem_bytes(in_dtype)) % 128 != 0));
     return mc ? 4 : 2;
 }
 
@@ -306,6 +311,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     const int pair = plan->pair;
+    if (pair == 2 && plan->multicast == 1 && plan->visible_devices != 1) return GEMM_ERR_UNSUPPORTED;
     const int cluster = unit_ctas(plan, K, dtype, layout);
     const int bn = choose_tile_n(plan, M, N, cluster, layout, batch.count);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
@@ -495,6 +501,7 @@ int gemm_plan_create(gemm_plan_t* out, int device, unsigned flags) {
     if (!plan) return GEMM_ERR_CUDA;
     plan->device = device;
     plan->sm_count = prop.multiProcessorCount;
+    plan->visible_devices = count;
     int rc = query_capacity(plan, 1);
     if (rc == GEMM_OK) rc = query_capacity(plan, 2);
     if (rc == GEMM_OK) rc = query_capacity(plan, 4);
@@ -564,6 +571,16 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             plan->fail_encode = (int)value;
             return GEMM_OK;
+        case GEMM_OPT_VISIBLE_DEVICES: {
+            if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
+            int n = (int)value;
+            if (n == 0 && cudaGetDeviceCount(&n) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            plan->visible_devices = n;
+            return GEMM_OK;
+        }
         case GEMM_OPT_TILE_N: {
             if (value == 0) {
                 plan->tile_n = 0;
@@ -898,8 +915,15 @@ void noalloc_setup(NoallocDevice* d, int device) {
         d->rc = GEMM_ERR_CUDA;
         return;
     }
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        cudaGetLastError();
+        d->rc = GEMM_ERR_CUDA;
+        return;
+    }
     d->state.device = device;
     d->state.sm_count = prop.multiProcessorCount;
+    d->state.visible_devices = count;
     d->state.d_status = static_cast<int*>(ptr);
     d->state.stream_k = 0;   // no workspace here: whole tiles only
     int rc = query_capacity(&d->state, 1);

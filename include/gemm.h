@@ -111,7 +111,10 @@ typedef enum {
                                     on vertically adjacent tiles and share their B tile
                                     through TMA multicast (512×BN per cluster); 0 = one
                                     pair per cluster; -1 (default) = multicast when the
-                                    rows of A and B are not a multiple of 128 bytes   */
+                                    rows of A and B are not a multiple of 128 bytes.
+                                    Multicast is used only while the process sees one
+                                    GPU (see GEMM_OPT_VISIBLE_DEVICES): with more, the
+                                    default picks pairs and 1 is GEMM_ERR_UNSUPPORTED */
     GEMM_OPT_WAIT_LIMIT_US = 7,  /* bound on any single wait inside the kernel, in µs,
                                     1..60e6 (0 = default: 2 s)                         */
     GEMM_OPT_STALL_TEST = 8,     /* tests of the timeout path only: 1 = the MMA warp
@@ -135,11 +138,21 @@ typedef enum {
                                     of tiles on (where it measured faster), else 0;
                                     0 on plans with GEMM_OPT_MAX_CTAS or
                                     GEMM_OPT_STREAM_K set                          */
-    GEMM_OPT_FAIL_ENCODE = 10    /* tests of the error path only: 1 = the driver's
+    GEMM_OPT_FAIL_ENCODE = 10,   /* tests of the error path only: 1 = the driver's
                                     tensor-map encoder is replaced by a fake that
                                     rejects the output map, so runs on this plan
                                     return GEMM_ERR_DRIVER before any launch and
                                     leave C untouched; 0 (default) = off            */
+    GEMM_OPT_VISIBLE_DEVICES = 11 /* GPUs the plan counts as visible to the process,
+                                    1..1024 (0 = default: cudaGetDeviceCount at plan
+                                    creation).  TMA multicast stays within one GPU's
+                                    own memory, and the library uses it only when a
+                                    single GPU is visible, so that no code of a
+                                    process that may drive several GPUs multicasts;
+                                    setting 2 or more here takes a one-GPU machine
+                                    through that rule (tests).  A plan that runs with
+                                    GEMM_OPT_MULTICAST = 1 returns GEMM_ERR_UNSUPPORTED
+                                    for a value above 1                            */
 } gemm_option_t;
 
 /* Create a plan for `device` (-1 = the current device); it becomes the plan

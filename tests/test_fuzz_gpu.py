@@ -65,6 +65,8 @@ def test_random_case_exact(g, i):
     As = [A_all[e * M:(e + 1) * M] for e in range(batch)]
     Bs = [B_all[e * N:(e + 1) * N] for e in range(batch)]
 
+    if c["unit"] == 4 and torch.cuda.device_count() > 1:
+        pytest.skip("the library multicasts only while one GPU is visible")
     plan = g.gemm_plan_create(0)
     try:
         g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 1 if c["unit"] == 1 else 2)

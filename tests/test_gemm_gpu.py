@@ -51,6 +51,8 @@ UNITS = [4, 2, 1]   # CTAs per work unit: multicast cluster of two pairs, one pa
 
 
 def configure(g, plan, unit):
+    if unit == 4 and torch.cuda.device_count() > 1:
+        pytest.skip("the library multicasts only while one GPU is visible")
     g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, 1 if unit == 1 else 2)
     g.gemm_plan_set_option(plan, g.GEMM_OPT_MULTICAST, 1 if unit == 4 else 0)
 
@@ -481,6 +483,44 @@ def test_host_threads_share_one_plan(g, fresh_plan):
     torch.cuda.synchronize()
     assert not errors, errors
     assert g.gemm_plan_status(fresh_plan) == 0
+
+
+def test_multicast_only_with_one_visible_gpu(g, fresh_plan):
+    """TMA multicast stays within one GPU's memory and the library uses it
+    only while the process sees a single GPU.  Rows of 1256 bf16 (2512
+    bytes, not a multiple of 128) make the default pick the 4-CTA multicast
+    unit with one GPU visible; counted as two, the same plan picks pairs
+    and refuses an explicit multicast request.  Results exact either way."""
+    M, N, K = 1000, 776, 1256
+    A, B = draw(M, N, K, dist="int", seed=77)
+    C_ref, _ = oracle_full(A, B)
+    Ad, Bd = A.cuda(), B.cuda()
+    opt = g.GEMM_OPT_VISIBLE_DEVICES
+    try:
+        for visible, unit in ((1, 4), (2, 2)):
+            g.gemm_plan_set_option(fresh_plan, opt, visible)
+            C = parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32))
+            assert g.gemm_plan_last_launch(fresh_plan)["ctas_per_unit"] == unit, visible
+            assert np.array_equal(C, C_ref), visible
+        g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MULTICAST, 1)
+        C = torch.full((M, N), float("nan"), device="cuda")
+        import ctypes
+        vp = ctypes.c_void_p
+        assert g.raw_status("gemm_plan_run", vp(fresh_plan), vp(Ad.data_ptr()), vp(Bd.data_ptr()), vp(C.data_ptr()),
+                            M, N, K, wl.BF16, wl.F32, None) == g.GEMM_ERR_UNSUPPORTED
+        torch.cuda.synchronize()
+        assert bool(torch.isnan(C).all()), "a refused run wrote C"
+        g.gemm_plan_set_option(fresh_plan, opt, 1)
+        C = parity.to_f64(run(g, fresh_plan, Ad, Bd, wl.F32))
+        assert g.gemm_plan_last_launch(fresh_plan)["ctas_per_unit"] == 4
+        assert np.array_equal(C, C_ref)
+    finally:
+        g.gemm_plan_set_option(fresh_plan, opt, 0)
+        g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_MULTICAST, -1)
+    for bad in (-1, 1025):
+        import ctypes
+        assert g.raw_status("gemm_plan_set_option", ctypes.c_void_p(fresh_plan), opt, ctypes.c_int64(bad)) \
+            == g.GEMM_ERR_INVALID_ARG
 
 
 def test_dynamic_and_static_agree(g, fresh_plan):
