@@ -31,6 +31,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxExtent = (int64_t(1) << 31) - 1024;   // largest M, N or K accepted
 
 std::mutex g_mu;
 std::vector<gemm_plan*> g_plans[kMaxDevices];  // live plans per device, newest last
@@ -171,7 +172,9 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    // The kernel's tile coordinates are 32-bit and run up to one tile past
+    // the last row, column or k-block: keep a margin below 2^31.
+    if (M > kMaxExtent || N > kMaxExtent || K > kMaxExtent) return GEMM_ERR_UNSUPPORTED;
     if (C == nullptr) return GEMM_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0) return GEMM_ERR_MISALIGNED;

@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // SM's TMA unit and shared memory with them.  Issued in
                     // one burst they slowed that K loop by a few percent
                     // (4096³: 77.7 -> 76.8 µs paced; E4M3 4096³ 45.6 -> 44.6).
-                    const uint32_t pace_ns = (uint32_t)min(2000, p.k_blocks * 256 / (3 * kChunks));
+                    const uint32_t pace_ns = (uint32_t)min(2000, min(p.k_blocks, 1 << 16) * 256 / (3 * kChunks));
                     uint32_t ra[32], rb[32];
                     tmem_ld_32x32b_x32(t_row, ra);
                     tmem_ld_wait(ra);

@@ -21,7 +21,8 @@
  *   - K * sizeof(input element) and N * sizeof(C element) bytes multiples
  *     of 16, i.e. K % 8 == 0 (bf16/f16 in) or K % 16 == 0 (fp8 in), and
  *     N % 8 == 0 (bf16/f16 out) or N % 4 == 0 (fp32 out);
- *   - M, N, K < 2^31.
+ *   - M, N, K <= 2^31 - 1024 (tile coordinates are 32-bit); larger sizes
+ *     return GEMM_ERR_UNSUPPORTED.
  * Other shapes return GEMM_ERR_UNSUPPORTED: there is no slow fallback path.
  *
  * Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 writes C = 0 (the

@@ -73,6 +73,10 @@ def test_host_validation_without_gpu(lib):
     assert rs("gemm_run", good, good, good, 64, 6, 64, 0, 0, None) == lib.GEMM_ERR_UNSUPPORTED
     assert rs("gemm_run", good, good, good, 64, 2, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
     assert rs("gemm_run", good, good, good, 1 << 31, 64, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+    for big in ((1 << 31) - 1016, 1 << 40):   # beyond the largest extent (2^31 - 1024) in M, N or K
+        assert rs("gemm_run", good, good, good, big, 64, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+        assert rs("gemm_run", good, good, good, 64, big, 64, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
+        assert rs("gemm_run", good, good, good, 64, 64, big, 0, 2, None) == lib.GEMM_ERR_UNSUPPORTED
     # empty problems are a no-op and touch nothing
     assert rs("gemm_run", None, None, None, 0, 64, 64, 0, 2, None) == lib.GEMM_OK
     assert rs("gemm_run", None, None, None, 64, 0, 64, 0, 2, None) == lib.GEMM_OK
