@@ -21,6 +21,7 @@
 #include "gemm.h"
 #include "gemm_kernel.cuh"
 #include "kernel_table.h"
+#include "launch_choice.h"
 
 namespace {
 
@@ -196,21 +197,17 @@ int max_resident_ctas(const gemm_plan* plan) {
     return std::max(plan->max_ctas[1], std::max(plan->max_ctas[2], plan->max_ctas[4]));
 }
 
-// CTAs per work unit: 1 (single CTA), 2 (a CTA pair) or 4 (two pairs
-// sharing B through TMA multicast).  Automatic choice: when the operand rows
-// are not a multiple of 128 bytes every 128-byte box row straddles an extra
-// 32-byte sector, the load path becomes the bound, and halving the B reads
-// wins (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of
-// all SMs wins (4-CTA clusters fit on 144 of the 152 SMs).
-// Multicast is used only while the process sees a single GPU (a process
-// that may drive several runs no multicast code at all); an explicit
-// request on a plan that sees more is refused in launch().
+// The launch shape: the decisions themselves live in launch_choice.h
+// (plain C++, also run by the CPU tests); these wrappers feed them the
+// plan's options and the resident-unit counts queried on the device.
+constexpr bool same_widths(int i = 0) {
+    return i == kNumTileWidths || (kLaunchWidths[i] == kTileWidths[i] && same_widths(i + 1));
+}
+static_assert(kLaunchTileWidths == kNumTileWidths && same_widths(), "tile widths: launch choice and kernel table agree");
+static_assert(kLaunchRowsPerCta == kRowsPerCta && kLaunchMnBox == kMnBoxElems, "launch choice and kernel agree");
+
 int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype, int layout) {
-    if (plan->pair != 2) return 1;
-    const bool mc = plan->visible_devices == 1 &&
-                    (plan->multicast == 1 ||
-                     (plan->multicast < 0 && layout == 0 && (K * elem_bytes(in_dtype)) % 128 != 0));
-    return mc ? 4 : 2;
+    return launch_unit_ctas(plan->pair, plan->multicast, plan->visible_devices, K, elem_bytes(in_dtype), layout);
 }
 
 // Resident units a launch may use.
@@ -220,86 +217,13 @@ int resident_units(const gemm_plan* plan, int cluster) {
     return std::max(1, units);
 }
 
-// With an MN-major B, whether every CTA's share of the tile's B rows (as
-// held for the MMA and as loaded) is whole 64-element TMA boxes.  If not, a
-// 1- or 2-CTA unit uses the padded kernel form (shares rounded up to whole
-// boxes); a 4-CTA unit cannot.
-bool b_boxes_exact(int bn, int cluster) {
-    const int pair = cluster >= 2 ? 2 : 1;
-    return (bn / pair) % kMnBoxElems == 0 && (bn / cluster) % kMnBoxElems == 0;
-}
-bool width_fits_layout(int bn, int cluster, int layout) {
-    return !(layout & GEMM_B_MN_MAJOR) || cluster <= 2 || b_boxes_exact(bn, cluster);
-}
-
-// Tile width: the candidate that minimises (waves of resident units) × (SM
-// cycles per k-block of that width), preferring the wider tile when two are
-// within 1%.  Cycles per k-block measured on GB300 at 8192³ (GEMM_TRACE
-// cycle stamps, steady state): CTA pairs (also the 4-CTA multicast unit)
-// 520 / 453 / 432 / 429 / 485 for widths 256 / 224 / 192 / 160 / 128 —
-// only 256 and 224 run at the MMA's own rate, narrower tiles hit a floor —
-// and single CTAs 673 / 652 / 528 / 506 / 482.  So 224 is picked at 4096³
-// (304 tiles = 4 whole waves on 76 pairs) and at 1024×4096×4096, 256 at
-// 8192³.  Returns 0 when no width fits (a forced width the layout cannot
-// use).
 int choose_tile_n(const gemm_plan* plan, int64_t M, int64_t N, int cluster, int layout, int64_t batch = 1) {
-    if (plan->tile_n > 0) return width_fits_layout(plan->tile_n, cluster, layout) ? plan->tile_n : 0;
-    static constexpr int64_t kCyclesPair[kNumTileWidths] = {520, 453, 432, 429, 485};
-    static constexpr int64_t kCyclesSingle[kNumTileWidths] = {673, 652, 528, 506, 482};
-    const int64_t* cycles = cluster >= 2 ? kCyclesPair : kCyclesSingle;
-    const int64_t units = resident_units(plan, cluster);
-    const int64_t tiles_m = batch * ((M + kRowsPerCta * cluster - 1) / (kRowsPerCta * cluster));
-    int best = 0;
-    int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < kNumTileWidths; ++i) {   // widest first
-        const int bn = kTileWidths[i];
-        if (!width_fits_layout(bn, cluster, layout)) continue;
-        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
-        const int64_t cost = ((tiles + units - 1) / units) * cycles[i];
-        if (cost * 100 < best_cost * 99) {   // a narrower tile must be > 1% cheaper
-            best_cost = cost;
-            best = bn;
-        }
-    }
-    return best;
+    return launch_tile_n(plan->tile_n, M, N, cluster, layout, batch, resident_units(plan, cluster));
 }
-
-// Dynamic work list of a launch (cluster launch control): `units`
-// persistent clusters with `waves` whole tiles each, then one single-tile
-// cluster per remaining tile.  Mode 1 hands out only the partial last
-// wave (the whole waves keep the static placement of tiles on SMs); mode 2
-// every tile.  Returns false for the static schedule: mode 0, or mode 1
-// when the tiles fill whole waves or fit in one.
-//
-// Automatic choice: mode 1 from kDynamicMinWaves whole waves on.  On GB300
-// some SMs run a 256-wide tile up to 4% slower than others (the same SMs in
-// every launch), so over many waves the static units drift apart and the
-// slowest one sets the end; handing out the partial last wave lets the
-// fast units take it.  Measured against the static schedule: 8192³ 588 →
-// 570 µs, 7168³ 389 → 384, 8192×8192×4096 291 → 286, 8192×4096×8192 294 →
-// 289, 5120³ 158 → 155 (6 to 13 waves); level at 3 to 5 waves; slower by
-// 1.5-4 µs at 1 or 2 waves (3072³, 3328×4096×4096, 4000×3000×5000), where
-// the drift is small and the handed-out tiles lose the static placement
-// (~5% slower per tile when every tile is handed out).  Mode 2 measured
-// slower than mode 1 almost everywhere.  Plans with a CTA cap or stream-K
-// keep the static schedule unless mode 1 or 2 is set explicitly.
-constexpr int64_t kDynamicMinWaves = 6;
 
 bool dynamic_lists(const gemm_plan* plan, int64_t tiles, int64_t resident, int* units, int* waves) {
-    int mode = plan->dynamic;
-    if (mode < 0)
-        mode = (plan->cap_ctas == 0 && !plan->stream_k && tiles / resident >= kDynamicMinWaves) ? 1 : 0;
-    if (mode == 2) {
-        *units = (int)tiles;
-        *waves = 1;
-        return true;
-    }
-    if (mode == 1 && tiles > resident && tiles % resident != 0) {
-        *units = (int)resident;
-        *waves = (int)(tiles / resident);
-        return true;
-    }
-    return false;
+    return launch_dynamic_lists(plan->dynamic, plan->cap_ctas > 0, plan->stream_k != 0, tiles, resident, units,
+                                waves);
 }
 
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
@@ -318,7 +242,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     const int cluster = unit_ctas(plan, K, dtype, layout);
     const int bn = choose_tile_n(plan, M, N, cluster, layout, batch.count);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
-    const bool pad = (layout & GEMM_B_MN_MAJOR) && !b_boxes_exact(bn, cluster);
+    const bool pad = (layout & GEMM_B_MN_MAJOR) && !launch_b_boxes_exact(bn, cluster);
     const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0, pad);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
     const int tile_m = kRowsPerCta * cluster;

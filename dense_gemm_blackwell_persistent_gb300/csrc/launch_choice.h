@@ -1,0 +1,126 @@
+// launch_choice.h -- how the host shapes a launch: CTAs per work unit, tile
+// width and the kind of work list.  Plain C++ (no CUDA calls), so that the
+// host code and the CPU tests run exactly the same decisions; gemm_api.cu
+// feeds them the plan's options and the resident-unit counts it queried on
+// the device.
+//
+// The measurements behind each rule are given with the rule.  The sources
+// for the rules themselves: whole waves of persistent units ("Collective
+// matrix multiplication": grid = number of SMs), 2-CTA pairs and clusters
+// sharing an operand by multicast ("Writing Mosaic GPU kernels with Pallas",
+// "Collective MMA", clusters and collective copies), and tiles handed out at
+// run time ("Writing Mosaic GPU kernels with Pallas", "Cluster launch
+// control").
+#pragma once
+#include <stdint.h>
+
+#include "gemm.h"
+
+namespace gb300 {
+
+constexpr int kLaunchTileWidths = 5;
+constexpr int kLaunchWidths[kLaunchTileWidths] = {256, 224, 192, 160, 128};   // widest first
+constexpr int kLaunchRowsPerCta = 128;   // rows of A per CTA (TMEM lanes)
+constexpr int kLaunchMnBox = 64;         // elements of M or N per MN-major TMA box
+
+// CTAs per work unit: 1 (pair = 1), 2 (a CTA pair) or 4 (two pairs sharing B
+// through TMA multicast).  Multicast is used only while the process sees
+// a single GPU, so no code of a process that may drive several GPUs
+// multicasts.  Automatic choice (multicast = -1): when the rows of K are not
+// a multiple of 128 bytes every 128-byte box row straddles an extra 32-byte
+// sector, the load path becomes the bound, and halving the B reads wins
+// (measured +29% at 4000×3000×5000); with aligned rows the pairs' use of all
+// SMs wins (4-CTA clusters fit on 144 of the 152 SMs).  An explicit request
+// for multicast that cannot be honoured is refused by the caller, not here.
+inline int launch_unit_ctas(int pair, int multicast, int visible_devices, int64_t K, int in_elem_bytes,
+                            int layout) {
+    if (pair != 2) return 1;
+    const bool mc = visible_devices == 1 &&
+                    (multicast == 1 || (multicast < 0 && layout == 0 && (K * in_elem_bytes) % 128 != 0));
+    return mc ? 4 : 2;
+}
+
+// With an MN-major B, whether every CTA's share of the tile's B rows (as
+// held for the MMA and as loaded) is whole 64-element TMA boxes.  If not, a
+// 1- or 2-CTA unit uses the padded kernel form (shares rounded up to whole
+// boxes); a 4-CTA unit cannot.
+inline bool launch_b_boxes_exact(int bn, int cluster) {
+    const int pair = cluster >= 2 ? 2 : 1;
+    return (bn / pair) % kLaunchMnBox == 0 && (bn / cluster) % kLaunchMnBox == 0;
+}
+inline bool launch_width_fits_layout(int bn, int cluster, int layout) {
+    return !(layout & GEMM_B_MN_MAJOR) || cluster <= 2 || launch_b_boxes_exact(bn, cluster);
+}
+
+// Tile width: the candidate that minimises (waves of resident units) × (SM
+// cycles per k-block of that width), preferring the wider tile when two are
+// within 1%.  Cycles per k-block measured on GB300 at 8192³ (GEMM_TRACE
+// cycle stamps, steady state): CTA pairs (also the 4-CTA multicast unit)
+// 520 / 453 / 432 / 429 / 485 for widths 256 / 224 / 192 / 160 / 128 —
+// only 256 and 224 run at (within ~3% of) the MMA's own rate, narrower tiles
+// wait on a ~460-cycle floor — and single CTAs 673 / 652 / 528 / 506 / 482.
+// So 224 is picked at 4096³ (304 tiles = 4 whole waves on 76 pairs) and at
+// 1024×4096×4096, 256 at 8192³.  `forced` > 0 is a width the caller asked
+// for.  `units`: resident units of this size.  Returns 0 when no width fits
+// (a forced width the layout cannot use).
+inline int launch_tile_n(int forced, int64_t M, int64_t N, int cluster, int layout, int64_t batch, int64_t units) {
+    if (forced > 0) return launch_width_fits_layout(forced, cluster, layout) ? forced : 0;
+    static constexpr int64_t kCyclesPair[kLaunchTileWidths] = {520, 453, 432, 429, 485};
+    static constexpr int64_t kCyclesSingle[kLaunchTileWidths] = {673, 652, 528, 506, 482};
+    const int64_t* cycles = cluster >= 2 ? kCyclesPair : kCyclesSingle;
+    if (units < 1) units = 1;
+    const int64_t tiles_m = batch * ((M + kLaunchRowsPerCta * cluster - 1) / (kLaunchRowsPerCta * cluster));
+    int best = 0;
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < kLaunchTileWidths; ++i) {   // widest first
+        const int bn = kLaunchWidths[i];
+        if (!launch_width_fits_layout(bn, cluster, layout)) continue;
+        const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + units - 1) / units) * cycles[i];
+        if (cost * 100 < best_cost * 99) {   // a narrower tile must be > 1% cheaper
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+// Dynamic work list of a launch (cluster launch control): `units`
+// persistent clusters with `waves` whole tiles each, then one single-tile
+// cluster per remaining tile.  Mode 1 hands out only the partial last
+// wave (the whole waves keep the static placement of tiles on SMs); mode 2
+// every tile.  Returns false for the static schedule: mode 0, or mode 1
+// when the tiles fill whole waves or fit in one.
+//
+// Automatic choice (mode -1): mode 1 from kDynamicMinWaves whole waves on.
+// On GB300 some SMs run a 256-wide tile up to 4% slower than others (the
+// same SMs in every launch), so over many waves the static units drift
+// apart and the slowest one sets the end; handing out the partial last wave
+// lets the fast units take it.  Measured against the static schedule:
+// 8192³ 588 → 570 µs, 7168³ 389 → 384, 8192×8192×4096 291 → 286,
+// 8192×4096×8192 294 → 289, 5120³ 158 → 155 (6 to 13 waves); level at 3 to
+// 5 waves; slower by 1.5-4 µs at 1 or 2 waves (3072³, 3328×4096×4096,
+// 4000×3000×5000), where the drift is small and the handed-out tiles lose
+// the static placement (~5% slower per tile when every tile is handed out).
+// Mode 2 measured slower than mode 1 almost everywhere.  Plans with a CTA
+// cap or stream-K keep the static schedule unless mode 1 or 2 is set
+// explicitly.
+constexpr int64_t kDynamicMinWaves = 6;
+
+inline bool launch_dynamic_lists(int mode, bool capped, bool stream_k, int64_t tiles, int64_t resident, int* units,
+                                 int* waves) {
+    if (mode < 0) mode = (!capped && !stream_k && tiles / resident >= kDynamicMinWaves) ? 1 : 0;
+    if (mode == 2) {
+        *units = (int)tiles;
+        *waves = 1;
+        return true;
+    }
+    if (mode == 1 && tiles > resident && tiles % resident != 0) {
+        *units = (int)resident;
+        *waves = (int)(tiles / resident);
+        return true;
+    }
+    return false;
+}
+
+}  // namespace gb300
