@@ -630,14 +630,18 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
     // chunk starts as soon as its rows are resident, and its rows of C go
     // back on another stream while later chunks are copied and computed.
     // Chunks are whole 256-row tiles (a CTA pair's tile height).  One chunk
-    // per 1024 rows, at most 8: smaller chunks shorten the tail (the last
-    // chunk's product and copy back), but below ~1024 rows a chunk's product
-    // no longer fills a wave of tiles.  The host link bounds it: measured on
+    // per 1024 rows, at most 8, and at least two from 512 rows on: smaller
+    // chunks shorten the tail (the last chunk's product and copy back), but
+    // below ~1024 rows a chunk's product no longer fills a wave of tiles and
+    // the extra copies and launches cost more than the tail saves (4096³:
+    // 8 chunks of 512 rows 293 vs 300 TFLOP/s end to end), except where one
+    // chunk would be the whole product (1024×4096×4096: 2 chunks 126 vs 118).  The host link bounds it: measured on
     // GB300 ~208 GB/s in and ~192 GB/s out one way at a time, ~165 GB/s each
     // way at once, the same whether the copy engines or SM loads and stores
     // move the bytes; 4096³ bf16 runs at ~300 TFLOP/s end to end (234
     // unpipelined), 8192³ at ~675.
-    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(8, M / 1024));
+    int64_t want = std::min<int64_t>(8, M / 1024);
+    if (want < 2) want = M >= 512 ? 2 : 1;
     int64_t rows = ((M + want - 1) / want + 255) / 256 * 256;
     const int nch = (int)((M + rows - 1) / rows);
     const size_t a_row_bytes = (size_t)K * elem_bytes(dtype), c_row_bytes = (size_t)N * elem_bytes(out_dtype);
