@@ -183,24 +183,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, smax, power, reasons = [], None, [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+        return summarise_clocks(self.lines)
+
+
+def summarise_clocks(lines):
+    """Median SM clock, maximum clock, throttle reasons seen and peak power from
+    `nvidia-smi --query-gpu=<ClockSampler.QUERY> --format=csv,noheader,nounits`
+    lines; lines that do not parse (a header, [N/A] fields) are skipped."""
+    sm, smax, power, reasons = [], None, [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            clock, top, watts = float(parts[1]), float(parts[2]), float(parts[3])
+        except ValueError:
+            continue
+        sm.append(clock)
+        smax = top
+        power.append(watts)
+        for nm, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+            "reasons": sorted(reasons), "samples": len(sm),
+            "power_w_max": max(power) if power else None}
 
 
 def cpu_baseline(w: wl.Workload, A_bits, B_bits, budget_s: float):

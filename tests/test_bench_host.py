@@ -69,3 +69,23 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"] == "gemm_256_f32out"
+
+
+def test_clock_summary_from_nvidia_smi_lines():
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = [
+        "index, clocks.current.sm [MHz], clocks.max.sm [MHz], power.draw [W], ...",   # a header: skipped
+        "0, 2070, 2070, 640.12, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1725, 2070, 1372.50, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1800, 2070, 1100.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, [N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",                      # unreadable: skipped
+        "0, 2070",                                                                          # truncated: skipped
+    ]
+    c = bench.summarise_clocks(lines)
+    assert c == {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3,
+                 "power_w_max": 1372.5}
+    throttled = bench.summarise_clocks([
+        "0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"])
+    assert throttled["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert bench.summarise_clocks([])["sm_mhz"] is None
