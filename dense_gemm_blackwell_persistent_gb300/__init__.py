@@ -216,6 +216,16 @@ def _dtype_code(t) -> int:
 _default_plans = {}
 
 
+def _check_devices(A, B):
+    """The library reads and writes device memory only: both operands must be
+    CUDA tensors on one device (a host pointer handed to the kernel would be
+    read as a device address)."""
+    if not (getattr(A, "is_cuda", False) and getattr(B, "is_cuda", False)):
+        raise ValueError("A and B must be CUDA tensors (gemm_plan_run_host takes host buffers)")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+
+
 def default_plan(device=None) -> int:
     """A plan for `device` (torch device or index; default: the current one),
     created on first use and kept for the life of the process; what
@@ -245,6 +255,7 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: boo
     Runs on torch's current stream of A's device.
     """
     import torch
+    _check_devices(A, B)
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be matrices")
     layout = (GEMM_A_MN_MAJOR if a_km else 0) | (GEMM_B_MN_MAJOR if b_kn else 0)
@@ -264,8 +275,8 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: boo
     N = B.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
-    elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [M,N] tensor of out_dtype")
+    elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous() or out.device != A.device:
+        raise ValueError("out must be a contiguous [M,N] tensor of out_dtype on A's device")
     stream = torch.cuda.current_stream(A.device).cuda_stream
     if plan is None:
         plan = default_plan(A.device)
@@ -284,8 +295,7 @@ def bmm(A, B, plan: Optional[int] = None, out_dtype=None, out=None):
     in one launch (gemm_plan_run_batched; plan: default_plan(A.device) when
     omitted).  Returns C [batch,M,N]."""
     import torch
-    if plan is None:
-        plan = default_plan(A.device)
+    _check_devices(A, B)
     if A.dim() not in (2, 3) or B.dim() not in (2, 3) or A.shape[-1] != B.shape[-1]:
         raise ValueError("A must be [batch,M,K] or [M,K], B [batch,N,K] or [N,K]")
     if A.dtype != B.dtype or not (A.is_contiguous() and B.is_contiguous()):
@@ -299,6 +309,10 @@ def bmm(A, B, plan: Optional[int] = None, out_dtype=None, out=None):
         out_dtype = A.dtype if A.element_size() == 2 else torch.bfloat16
     if out is None:
         out = torch.empty((batch, M, N), dtype=out_dtype, device=A.device)
+    elif out.shape != (batch, M, N) or out.dtype != out_dtype or not out.is_contiguous() or out.device != A.device:
+        raise ValueError("out must be a contiguous [batch,M,N] tensor of out_dtype on A's device")
+    if plan is None:
+        plan = default_plan(A.device)
     sa = M * K if A.dim() == 3 else 0
     sb = N * K if B.dim() == 3 else 0
     gemm_plan_run_batched(plan, A.data_ptr(), B.data_ptr(), out.data_ptr(), batch, M, N, K, sa, sb, M * N,

@@ -118,3 +118,18 @@ def test_product_path_has_no_cpu_fallback():
         assert "oracle" not in text.replace("oracle/", ""), path
         for forbidden in ("torch.matmul", "np.matmul", "np.dot", "einsum", "torch.mm("):
             assert forbidden not in text, (path, forbidden)
+
+
+def test_torch_helpers_refuse_host_tensors(lib):
+    """matmul() and bmm() hand device pointers to the library: host tensors are
+    refused before anything reaches it (they would be read as device
+    addresses); host buffers go through gemm_plan_run_host instead."""
+    import torch
+    A = torch.zeros((64, 64), dtype=torch.bfloat16)
+    B = torch.zeros((32, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.matmul(A, B)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.matmul(A, B.t().contiguous(), b_kn=True)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.bmm(A.view(1, 64, 64), B)
