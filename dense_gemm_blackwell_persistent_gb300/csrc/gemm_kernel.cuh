@@ -17,7 +17,8 @@
 //               the mbarriers.
 //   warps 2..5  epilogue: TMEM -> registers -> swizzled shared staging ->
 //               TMA store in 32-column boxes, while the MMA thread already
-//               fills the other accumulator with the next tile.
+//               fills the other accumulator with the next tile (the stores
+//               paced over that tile's K loop).
 //
 // The tile width kBN (256, 224, 192, 160 or 128) is chosen per problem on
 // the host so that the tile count fills whole waves of resident CTA pairs.
@@ -804,8 +805,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     // them over about a third of the next tile's K loop
                     // (~256 ns per k-block), whose operand loads share the
                     // SM's TMA unit and shared memory with them.  Issued in
-                    // one burst they slowed that K loop by a few percent
-                    // (4096³: 77.7 -> 76.8 µs paced; E4M3 4096³ 45.6 -> 44.6).
+                    // one burst they slowed that K loop by 1-2% (4096³:
+                    // 77.7 -> 76.8 µs paced; E4M3 4096³ 45.6 -> 44.6).
                     const uint32_t pace_ns = (uint32_t)min(2000, min(p.k_blocks, 1 << 16) * 256 / (3 * kChunks));
                     uint32_t ra[32], rb[32];
                     tmem_ld_32x32b_x32(t_row, ra);
