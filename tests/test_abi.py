@@ -44,11 +44,6 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(raw, name), f"{name} declared in include/ but not exported"
 
 
-def test_library_is_native_sm103a(lib):
-    data = open(lib.LIB_PATH, "rb").read()
-    assert b"sm_103a" in data or b"sm_103" in data
-
-
 def test_host_validation_without_gpu(lib):
     vp = ctypes.c_void_p
     rs = lib.raw_status

@@ -1,5 +1,7 @@
 """Build properties of the kernel, checked without a GPU: ptxas's own report
-(-Xptxas -v: registers, stack, spills) for representative instantiations.
+(-Xptxas -v: target, registers, stack, spills) for representative
+instantiations.  The report names the target each entry function was
+assembled for, which must be sm_103a.
 
 The persistent kernel keeps one CTA per SM with 192 threads, so registers
 are not what limits residency, but a spill would put local-memory traffic
@@ -46,7 +48,9 @@ def test_no_spills_in_the_kernel(tmp_path):
     with ThreadPoolExecutor(len(CASES)) as ex:
         reports = list(ex.map(lambda c: _ptxas_report(c, str(tmp_path)), CASES))
     for case, rep in zip(CASES, reports):
-        entries = re.findall(r"Compiling entry function '(\w+)'", rep)
+        entries = re.findall(r"Compiling entry function '(\w+)' for '(sm_\w+)'", rep)
+        assert entries and all(arch == "sm_103a" for _, arch in entries), (case, entries)
+        entries = [name for name, _ in entries]
         frames = re.findall(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", rep)
         regs = [int(r) for r in re.findall(r"Used (\d+) registers", rep)]
         assert entries and len(frames) == len(entries) == len(regs), (case, rep[-2000:])
