@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--dynamic", type=int, default=-1, help="-1 auto, 0 static, 1 hand out the partial wave, 2 every tile")
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core issue-rate probe")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the context lines (L2-resident run, other workloads, sustained runs)")
+    ap.add_argument("--sustained-s", type=float, default=4.0, help="seconds of each sustained run (0 = none)")
     return ap.parse_args()
 
 
@@ -237,6 +240,20 @@ def cpu_baseline(w: wl.Workload, A_bits, B_bits, budget_s: float):
                       f"fp64 triple loop incl. operand decode"}
 
 
+def cpu_single_thread_256():
+    """The oracle on one thread for the 256³ workload (whole product)."""
+    import oracle
+    w1 = wl.WORKLOADS["gemm_256_f32out"]
+    A, B = wl.make_inputs(w1)
+    Ab, Bb = wl.as_bits(A), wl.as_bits(B)
+    oracle.gemm(Ab[:8], Bb, w1.dtype, threads=1)
+    t0 = time.perf_counter()
+    oracle.gemm(Ab, Bb, w1.dtype, threads=1)
+    dt = time.perf_counter() - t0
+    return {"value": w1.flops / dt / 1e12, "unit": "TFLOP/s", "seconds": dt, "cores": 1,
+            "sample": "the whole 256x256x256 product, fp64 triple loop incl. operand decode, 1 thread"}
+
+
 def run_reference(args, w: wl.Workload):
     rank, _, world = dist_info()
     if world > 1 and rank != 0:
@@ -274,6 +291,238 @@ def run_reference(args, w: wl.Workload):
     print(json.dumps(line), flush=True)
 
 
+# The other workloads of the benchmark set, each timed briefly in the same
+# process after the main one (their lines go under "other_workloads").
+OTHER_WORKLOADS = ["gemm_256_f32out", "gemm_1024x4096x4096_f16", "gemm_ragged_4000x3000x5000", "gemm_8192_bf16",
+                   "gemm_4096_e4m3"]
+SUSTAINED_WORKLOADS = ["gemm_4096_bf16", "gemm_8192_bf16"]
+
+
+def make_plan(g, args, device):
+    plan = g.gemm_plan_create(device)
+    if args.cta_pair:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, args.cta_pair)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_DYNAMIC, args.dynamic)
+    if args.group_m:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_GROUP_M, args.group_m)
+    if args.tile_n:
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_TILE_N, args.tile_n)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_MULTICAST, args.multicast)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_STREAM_K, args.stream_k)
+    return plan
+
+
+def kernel_clock(records):
+    """SM clock of the timed launches from the plan's clock log: per launch
+    cycles ÷ ns of its first CTA's lifetime, summarised."""
+    mhz = [c / ns * 1e3 for c, ns in records if ns > 0]
+    if not mhz:
+        return None
+    return {"sm_mhz_median": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+            "launches": len(mhz),
+            "how": "clock64 and %globaltimer at entry and exit of each launch's first CTA (GEMM_OPT_CLOCK_LOG)"}
+
+
+def tensor_peak(peaks, dtype):
+    """The measured dense peak for the operand type, and where it comes from."""
+    peak = float(peaks["bf16_tflops"])
+    note = "MEASURED_PEAKS bf16_tflops (burst, cuBLAS 8192^3)"
+    if dtype in wl.FP8:
+        # no measured fp8 figure: the bf16 one times the nominal dense ratio 4.5 / 2.25
+        peak *= 2.0
+        note += " x 2 (nominal fp8:bf16 dense ratio)"
+    return peak, note
+
+
+def roofline(w, achieved_tflops, mean_ms, peaks, peak_src, probe, sms, clock):
+    """Roofline of one launch: the bound is the slower of the FLOPs at the
+    measured tensor peak and the compulsory bytes at the measured HBM copy
+    bandwidth; achieved and peak are in that bound's unit.  Also the fraction
+    of the tensor cores' own rate at the maximum SM clock and at the clock the
+    launches ran at (issue-rate probe × SMs × clock)."""
+    peak, note = tensor_peak(peaks, w.dtype)
+    hbm = float(peaks["hbm_gbs"])
+    t_flop = w.flops / (peak * 1e12)
+    t_mem = w.compulsory_bytes / (hbm * 1e9)
+    bound = "tensor" if t_flop >= t_mem else "hbm"
+    if bound == "tensor":
+        out = {"bound": bound, "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
+               "frac": achieved_tflops / peak}
+    else:
+        gbs = w.compulsory_bytes / (mean_ms / 1e3) / 1e9
+        out = {"bound": bound, "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
+    out["peak_source"] = f"{peak_src}: " + (note if bound == "tensor" else "MEASURED_PEAKS hbm_gbs (copy)")
+    out["terms_us"] = {"flops_at_peak": t_flop * 1e6, "compulsory_bytes_at_hbm": t_mem * 1e6}
+    if probe is not None:
+        per_clk = probe["flop_per_clk_per_sm"]
+        at_max = per_clk * sms * float(peaks.get("sm_max_mhz", 2070.0)) / 1e6
+        out["peak_clock_tflops"] = at_max
+        out["frac_peak_clock"] = achieved_tflops / at_max
+        if clock is not None:
+            at_run = per_clk * sms * clock["sm_mhz_median"] / 1e6
+            out["kernel_clock_tflops"] = at_run
+            out["frac_kernel_clock"] = achieved_tflops / at_run
+        out["peak_clock_how"] = ("tcgen05.mma issue-rate probe (FLOP per SM clock, measured) x SMs x "
+                                 "MEASURED_PEAKS sm_max_mhz; kernel clock: the timed launches' own")
+    return out
+
+
+def cublas_call(torch, w, A, B, out_t):
+    """The cuBLAS reference for workload w (same inputs, same output type), or
+    (None, reason)."""
+    if w.dtype in wl.FP8:
+        if not hasattr(torch, "_scaled_mm"):
+            return None, "torch._scaled_mm missing"
+        one = torch.ones((), dtype=torch.float32, device="cuda")
+        return (lambda: torch._scaled_mm(A, B.t(), scale_a=one, scale_b=one, out_dtype=out_t)), \
+            "torch._scaled_mm(A, B.t(), unit scales)"
+    Bt = B.t()
+    if w.out_dtype == w.dtype:
+        return (lambda: torch.matmul(A, Bt)), "torch.matmul(A, B.t())"
+    return (lambda: torch.mm(A, Bt, out_dtype=out_t)), "torch.mm(A, B.t(), out_dtype=float32)"
+
+
+def time_cublas(torch, w, call, how, stream, flush, runs=50):
+    try:
+        for _ in range(5):
+            call()
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(runs)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(runs)]
+        # Same protocol as the timed steps: events around each launch on the
+        # stream, no host synchronisation inside the loop.
+        for i in range(runs):
+            if flush is not None:
+                flush.zero_()
+            cs[i].record(stream)
+            call()
+            ce[i].record(stream)
+        torch.cuda.synchronize()
+    except (RuntimeError, NotImplementedError, TypeError) as e:   # no such path in this torch build
+        return {"unavailable": f"{how}: " + str(e).splitlines()[0][:200]}
+    cm = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
+    l2 = "L2 flushed" if flush is not None else "L2 not flushed"
+    return {"value": w.flops / (cm / 1e3) / 1e12, "unit": "TFLOP/s", "ms": cm,
+            "how": f"{how}, same inputs, same process, {runs} runs, {l2}"}
+
+
+def time_launches(torch, g, plan, w, A, B, C, stream, steps, warmup, flush, barrier=None):
+    """CUDA events around each of `steps` launches on `stream` (after `warmup`
+    untimed ones), L2 flushed before each step when `flush` is a buffer; the
+    timed loop is bracketed by `barrier()` (all ranks) and a device
+    synchronisation on both sides.  Returns the per-launch times (ms), the
+    clock log of the timed launches and the host wall time of the timed loop."""
+    sp = stream.cuda_stream
+
+    def step():
+        g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype, sp)
+
+    for _ in range(max(3, warmup)):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if g.gemm_plan_status(plan) != 0:
+        raise SystemExit(f"{w.name}: device status error during warm-up")
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_CLOCK_LOG, steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if barrier is not None:
+        barrier()
+    status = g.gemm_plan_status(plan)
+    if status != 0:
+        raise SystemExit(f"{w.name}: device status {status} after the timed region")
+    records = g.gemm_plan_clock_log(plan, capacity=steps)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_CLOCK_LOG, 0)
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], records, wall
+
+
+def other_workload_line(torch, g, args, name, peaks, peak_src, probe_rates, sms, stream, flush, local):
+    """Short flushed run of one more workload: TFLOP/s, roofline, kernel clock,
+    launch shape and the cuBLAS line on the same inputs."""
+    w = wl.WORKLOADS[name]
+    A_cpu, B_cpu = wl.make_inputs(w)
+    A, B = A_cpu.cuda(), B_cpu.cuda()
+    out_t = wl.TORCH_DTYPES[w.out_dtype]
+    C = torch.empty((w.M, w.N), dtype=out_t, device="cuda")
+    plan = make_plan(g, args, local)
+    try:
+        steps = 200 if w.flops < 1e11 else 50
+        ms, records, _ = time_launches(torch, g, plan, w, A, B, C, stream, steps, 5, flush)
+        launch = g.gemm_plan_last_launch(plan)
+    finally:
+        g.gemm_plan_destroy(plan)
+    mean_ms = statistics.mean(ms)
+    achieved = w.flops / (mean_ms / 1e3) / 1e12
+    clock = kernel_clock(records)
+    line = {"value": achieved, "unit": "TFLOP/s", "steps": steps, "ms_mean": mean_ms, "ms_min": min(ms),
+            "ms_median": statistics.median(ms), "launch": launch, "kernel_clock": clock,
+            "roofline": roofline(w, achieved, mean_ms, peaks, peak_src, probe_rates.get(w.dtype), sms, clock),
+            "config": {"M": w.M, "N": w.N, "K": w.K, "in": wl.DTYPE_NAMES[w.dtype],
+                       "out": wl.DTYPE_NAMES[w.out_dtype], "inputs": w.describe()}}
+    line["roofline"]["traffic"] = recorded_traffic(w.name, launch)
+    if not args.no_cublas:
+        call, how = cublas_call(torch, w, A, B, out_t)
+        line["cublas_reference"] = time_cublas(torch, w, call, how, stream, flush) if call else {"unavailable": how}
+    return line
+
+
+def sustained_line(torch, g, args, name, seconds, stream, local):
+    """Back-to-back launches for about `seconds` (no flush: MEASURED_PEAKS'
+    sustained method, operands resident), one pair of events around the
+    whole loop; the launches' own clock and nvidia-smi's beside it."""
+    w = wl.WORKLOADS[name]
+    A_cpu, B_cpu = wl.make_inputs(w)
+    A, B = A_cpu.cuda(), B_cpu.cuda()
+    C = torch.empty((w.M, w.N), dtype=wl.TORCH_DTYPES[w.out_dtype], device="cuda")
+    plan = make_plan(g, args, local)
+    sp = stream.cuda_stream
+    try:
+        def step():
+            g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype,
+                            sp)
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 20
+        n = max(20, int(seconds / per))
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_CLOCK_LOG, n)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.25)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        smi = sampler.stop()
+        if g.gemm_plan_status(plan) != 0:
+            raise SystemExit(f"{name}: device status error in the sustained run")
+        records = g.gemm_plan_clock_log(plan, capacity=n)
+    finally:
+        g.gemm_plan_destroy(plan)
+    ms = ev0.elapsed_time(ev1)
+    return {"value": w.flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n, "seconds": ms / 1e3,
+            "kernel_clock": kernel_clock(records), "clocks": smi,
+            "how": "back-to-back launches, operands resident (no flush), events around the whole loop"}
+
+
 def main():
     args = parse_args()
     w = wl.WORKLOADS[args.workload]
@@ -289,17 +538,7 @@ def main():
     torch.cuda.set_device(local)
     import dense_gemm_blackwell_persistent_gb300 as g
 
-    plan = g.gemm_plan_create(local)
-    if args.cta_pair:
-        g.gemm_plan_set_option(plan, g.GEMM_OPT_CTA_PAIR, args.cta_pair)
-    g.gemm_plan_set_option(plan, g.GEMM_OPT_DYNAMIC, args.dynamic)
-    if args.group_m:
-        g.gemm_plan_set_option(plan, g.GEMM_OPT_GROUP_M, args.group_m)
-    if args.tile_n:
-        g.gemm_plan_set_option(plan, g.GEMM_OPT_TILE_N, args.tile_n)
-    g.gemm_plan_set_option(plan, g.GEMM_OPT_MULTICAST, args.multicast)
-    g.gemm_plan_set_option(plan, g.GEMM_OPT_STREAM_K, args.stream_k)
-
+    plan = make_plan(g, args, local)
     A_cpu, B_cpu = wl.make_inputs(w)
     A, B = A_cpu.cuda(), B_cpu.cuda()
     out_t = wl.TORCH_DTYPES[w.out_dtype]
@@ -307,104 +546,42 @@ def main():
     flush = None if args.no_flush else torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
-    def step():
-        g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype, sp)
-
-    for _ in range(max(3, args.warmup)):
-        if flush is not None:
-            flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    if g.gemm_plan_status(plan) != 0:
-        raise SystemExit("device status error during warm-up")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
+    barrier = torch.distributed.barrier if world > 1 else None
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if world > 1:
-        torch.distributed.barrier()
+    launch_ms, records, wall = time_launches(torch, g, plan, w, A, B, C, stream, args.steps, args.warmup, flush,
+                                             barrier)
     clocks = sampler.stop()
-    status = g.gemm_plan_status(plan)
-    if status != 0:
-        raise SystemExit(f"device status {status} after the timed region")
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks["in_kernel"] = kernel_clock(records)
     value, ms_per_step = aggregate(world, w.flops, args.steps, sum(launch_ms))
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = w.flops / (avg_launch_ms / 1e3) / 1e12
+    timed_launch = g.gemm_plan_last_launch(plan)   # before the e2e runs launch other shapes
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
-    peak_note = f"{peak_src}: MEASURED_PEAKS bf16_tflops (burst, cuBLAS 8192^3)"
-    if w.dtype in wl.FP8:
-        # no measured fp8 figure: the bf16 one times the nominal dense ratio 4.5 / 2.25
-        peak *= 2.0
-        peak_note += " x 2 (nominal fp8:bf16 dense ratio)"
-    timed_launch = g.gemm_plan_last_launch(plan)   # before the e2e runs launch other shapes
-    traffic = recorded_traffic(w.name, timed_launch)
+    # The tensor cores' own rate, measured by a stream of back-to-back MMAs of
+    # this kernel's shape with no loads, on every SM, after the timed region
+    # (outside it): per operand width, for the roofline at a given clock.
+    probe_rates = {}
+    if rank == 0 and not args.no_probe:
+        for dt in sorted({w.dtype, wl.BF16, wl.F16, wl.E4M3}):
+            probe_rates[dt] = g.gemm_probe_mma_rate(dt, args.cta_pair or 2, 1 << 16)
+    probe = probe_rates.get(w.dtype)
+    roof = roofline(w, achieved, avg_launch_ms, peaks, peak_src, probe, sms, clocks["in_kernel"])
+    roof["traffic"] = recorded_traffic(w.name, timed_launch)
+    if probe is not None:
+        roof["mma_probe"] = {"tflops": probe["tflops"], "sm_mhz": probe["sm_mhz"],
+                             "flop_per_clk_per_sm": probe["flop_per_clk_per_sm"], "frac": achieved / probe["tflops"],
+                             "how": "gemm_probe_mma_rate: 65536 back-to-back tcgen05.mma per SM, operands in "
+                                    "shared memory, no loads; frac = achieved / tflops at the probe's own clock"}
 
     extra = {}
-    ref_call, ref_how = None, None
-    if w.dtype in wl.FP8:
-        one = torch.ones((), dtype=torch.float32, device="cuda")
-        if hasattr(torch, "_scaled_mm"):
-            ref_call = lambda: torch._scaled_mm(A, B.t(), scale_a=one, scale_b=one, out_dtype=out_t)
-            ref_how = "torch._scaled_mm(A, B.t(), unit scales, out bf16)"
-    elif w.out_dtype == w.dtype:
-        Bt = B.t()
-        ref_call = lambda: torch.matmul(A, Bt)
-        ref_how = "torch.matmul(A, B.t())"
-    if not args.no_cublas and rank == 0 and ref_call is not None:
-        try:
-            for _ in range(5):
-                ref_call()
-            # Same protocol as the timed steps: events around each launch on
-            # the stream, no host synchronisation inside the loop (a host
-            # wait per run would put the next launch's host-side latency
-            # inside its events whenever no flush is queued ahead of it).
-            cs = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
-            ce = [torch.cuda.Event(enable_timing=True) for _ in range(50)]
-            for i in range(50):
-                if flush is not None:
-                    flush.zero_()
-                cs[i].record(stream)
-                ref_call()
-                ce[i].record(stream)
-            torch.cuda.synchronize()
-            cm = statistics.mean(a.elapsed_time(b) for a, b in zip(cs, ce))
-            l2 = "L2 flushed" if flush is not None else "L2 not flushed"
-            extra["cublas_reference"] = {"value": w.flops / (cm / 1e3) / 1e12, "unit": "TFLOP/s", "ms": cm,
-                                         "how": f"{ref_how}, same inputs, same process, 50 runs, {l2}"}
-        except RuntimeError as e:   # a torch build without this fp8 path: no reference line
-            extra["cublas_reference"] = {"unavailable": str(e).splitlines()[0][:200]}
-
-    # Context for the roofline: the tensor cores' own rate, measured by a
-    # stream of back-to-back MMAs of this kernel's shape with no loads, on
-    # every SM, right after the timed region (outside it).
-    mma_probe = None
-    if rank == 0 and not args.no_probe:
-        r = g.gemm_probe_mma_rate(w.dtype, args.cta_pair or 2, 1 << 16)
-        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        mma_probe = {"tflops": r["tflops"], "sm_mhz": r["sm_mhz"], "flop_per_clk_per_sm": r["flop_per_clk_per_sm"],
-                     "frac": achieved / r["tflops"],
-                     "peak_at_max_clock_tflops":
-                         r["flop_per_clk_per_sm"] * sms * float(peaks.get("sm_max_mhz", 2070.0)) / 1e6,
-                     "how": "gemm_probe_mma_rate: 65536 back-to-back tcgen05.mma per SM, operands in shared memory, "
-                            "no loads; frac = achieved / tflops"}
+    if not args.no_cublas and rank == 0:
+        call, how = cublas_call(torch, w, A, B, out_t)
+        extra["cublas_reference"] = time_cublas(torch, w, call, how, stream, flush) if call else {"unavailable": how}
 
     e2e = None
     if not args.no_e2e:
@@ -422,12 +599,40 @@ def main():
         e2e = {"value": e2e_value, "unit": "TFLOP/s",
                "h2d_bytes_per_step": (w.M + w.N) * w.K * wl.ELEM_BYTES[w.dtype],
                "d2h_bytes_per_step": w.M * w.N * wl.ELEM_BYTES[w.out_dtype],
-               "how": "gemm_plan_run_host: pinned host A,B in, host C out, row chunks with copies in, products and copies back overlapped on the plan's streams, sync per step, "
+               "how": "gemm_plan_run_host: pinned host A,B in, host C out, row chunks with copies in, products and "
+                      "copies back overlapped on the plan's streams, sync per step, "
                       f"host wall clock, {args.e2e_steps} steps"}
+    g.gemm_plan_destroy(plan)
+
+    # Context lines, outside the timed region (rank 0 only): the same
+    # workload with L2 left warm between launches, the other workloads of the
+    # benchmark set, and seconds-long back-to-back runs at the power limit.
+    if rank == 0 and not args.no_extra:
+        resident = g.gemm_plan_create(local)
+        try:
+            ms_res, rec_res, _ = time_launches(torch, g, resident, w, A, B, C, stream, 200, 5, None)
+        finally:
+            g.gemm_plan_destroy(resident)
+        extra["l2_resident"] = {"value": w.flops / (statistics.mean(ms_res) / 1e3) / 1e12, "unit": "TFLOP/s",
+                                "ms_mean": statistics.mean(ms_res), "kernel_clock": kernel_clock(rec_res),
+                                "how": "200 launches, no flush between them (operands stay in L2), default plan"}
+        del A, B, C
+        others = {}
+        for name in OTHER_WORKLOADS:
+            if name != w.name:
+                others[name] = other_workload_line(torch, g, args, name, peaks, peak_src, probe_rates, sms, stream,
+                                                   flush, local)
+        extra["other_workloads"] = others
+        if args.sustained_s > 0:
+            extra["sustained"] = {name: sustained_line(torch, g, args, name, args.sustained_s, stream, local)
+                                  for name in SUSTAINED_WORKLOADS}
+            extra["sustained"]["reference"] = {"bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"),
+                                               "source": f"{peak_src}: MEASURED_PEAKS (cuBLAS 8192^3, 4 s)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, wl.as_bits(A_cpu), wl.as_bits(B_cpu), args.cpu_seconds)
+        cpu["single_thread_256"] = cpu_single_thread_256()
 
     if rank == 0:
         line = {
@@ -443,9 +648,7 @@ def main():
                        "tile_per_mma": f"{128 * (args.cta_pair or 2)}x{timed_launch['tile_n']}x"
                                        f"{128 // wl.ELEM_BYTES[w.dtype]}",
                        "vs_baseline_ref": "pages' 293.6 TFLOP/s, Mojo part-2 kernel 4 on B200 (context)"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": peak_note, "mma_probe": mma_probe},
+            "roofline": roof,
             "clocks": clocks,
             "gpu_launches": args.steps,
             "e2e": e2e,
@@ -455,7 +658,6 @@ def main():
         }
         line.update(extra)
         print(json.dumps(line), flush=True)
-    g.gemm_plan_destroy(plan)
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -27,6 +27,7 @@ GEMM_ERR_DRIVER = -5
 GEMM_ERR_NO_PLAN = -6
 GEMM_ERR_TIMEOUT = -7
 GEMM_ERR_NO_DEVICE = -8
+GEMM_ERR_INTERNAL = -9
 GEMM_OPT_CTA_PAIR, GEMM_OPT_GROUP_M, GEMM_OPT_MAX_CTAS, GEMM_OPT_TILE_N, GEMM_OPT_STREAM_K = 1, 2, 3, 4, 5
 GEMM_OPT_MULTICAST = 6
 GEMM_OPT_WAIT_LIMIT_US = 7
@@ -34,9 +35,11 @@ GEMM_OPT_STALL_TEST = 8
 GEMM_OPT_DYNAMIC = 9
 GEMM_OPT_FAIL_ENCODE = 10
 GEMM_OPT_VISIBLE_DEVICES = 11
+GEMM_OPT_CLOCK_LOG = 12
 GEMM_K_MAJOR, GEMM_A_MN_MAJOR, GEMM_B_MN_MAJOR = 0, 1, 2
 
-# GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps).
+# GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps),
+# GB300_GEMM_VARIANT=debug the GEMM_DEBUG build (consistency checks in the kernel).
 VARIANT = os.environ.get("GB300_GEMM_VARIANT", "")
 LIB_PATH = _build.lib_path(VARIANT)
 
@@ -46,7 +49,8 @@ if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: {_REBUILD}")
 
 _lib = ctypes.CDLL(LIB_PATH)
-_missing = [n for n in ("gemm_plan_create", "gemm_plan_run_batched", "gemm_probe_mma_rate_n", "gemm_run_noalloc")
+_missing = [n for n in ("gemm_plan_create", "gemm_plan_run_batched", "gemm_probe_mma_rate_n", "gemm_run_noalloc",
+                        "gemm_plan_clock_log")
             if not hasattr(_lib, n)]
 if _missing:
     raise ImportError(f"{LIB_PATH} is out of date (no {', '.join(_missing)}): {_REBUILD}")
@@ -69,6 +73,7 @@ _lib.gemm_plan_last_tile_n.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_launch.argtypes = [_vp] + [ctypes.POINTER(_int)] * 5
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]
+_lib.gemm_plan_clock_log.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint64), _i64, ctypes.POINTER(_i64)]
 _lib.gemm_probe_mma_rate.argtypes = [_int, _int, _i64] + [ctypes.POINTER(ctypes.c_double)] * 3
 _lib.gemm_probe_mma_rate_n.argtypes = [_int, _int, _int, _i64] + [ctypes.POINTER(ctypes.c_double)] * 3
 _lib.gemm_strerror.argtypes = [_int]
@@ -76,7 +81,8 @@ _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_run_batched", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
               "gemm_plan_last_launch",
-              "gemm_plan_trace", "gemm_plan_destroy", "gemm_probe_mma_rate", "gemm_probe_mma_rate_n"):
+              "gemm_plan_trace", "gemm_plan_clock_log", "gemm_plan_destroy", "gemm_probe_mma_rate",
+              "gemm_probe_mma_rate_n"):
     getattr(_lib, _name).restype = _int
 
 
@@ -192,6 +198,15 @@ def gemm_plan_trace(plan: int):
     return buf
 
 
+def gemm_plan_clock_log(plan: int, capacity: int = 1 << 16) -> list:
+    """(SM cycles, ns) of CTA 0's lifetime for each launch since the last
+    read, oldest first (GEMM_OPT_CLOCK_LOG must be set); empties the log."""
+    buf = (ctypes.c_uint64 * (2 * capacity))()
+    n = _i64(0)
+    _check(_lib.gemm_plan_clock_log(_vp(plan), buf, capacity, ctypes.byref(n)), "gemm_plan_clock_log")
+    return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n.value)]
+
+
 def gemm_plan_destroy(plan: int) -> None:
     _check(_lib.gemm_plan_destroy(_vp(plan)), "gemm_plan_destroy")
 
@@ -282,10 +297,11 @@ def matmul(A, B, out_dtype=None, plan: Optional[int] = None, out=None, a_km: boo
         plan = default_plan(A.device)
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, _dtype_code(A.dtype),
             _dtype_code(out_dtype), stream)
-    if layout:
-        gemm_plan_run_layout(plan, *args[:-1], layout, args[-1])
-    else:
-        gemm_plan_run(plan, *args)
+    with torch.cuda.device(A.device):   # the library runs on the current device: the operands'
+        if layout:
+            gemm_plan_run_layout(plan, *args[:-1], layout, args[-1])
+        else:
+            gemm_plan_run(plan, *args)
     return out
 
 
@@ -315,7 +331,8 @@ def bmm(A, B, plan: Optional[int] = None, out_dtype=None, out=None):
         plan = default_plan(A.device)
     sa = M * K if A.dim() == 3 else 0
     sb = N * K if B.dim() == 3 else 0
-    gemm_plan_run_batched(plan, A.data_ptr(), B.data_ptr(), out.data_ptr(), batch, M, N, K, sa, sb, M * N,
-                          _dtype_code(A.dtype), _dtype_code(out_dtype), 0,
-                          torch.cuda.current_stream(A.device).cuda_stream)
+    with torch.cuda.device(A.device):
+        gemm_plan_run_batched(plan, A.data_ptr(), B.data_ptr(), out.data_ptr(), batch, M, N, K, sa, sb, M * N,
+                              _dtype_code(A.dtype), _dtype_code(out_dtype), 0,
+                              torch.cuda.current_stream(A.device).cuda_stream)
     return out

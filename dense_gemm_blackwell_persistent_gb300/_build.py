@@ -22,8 +22,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libgb300gemm.so")
 # Build variants: "" is the product library; "trace" adds -DGEMM_TRACE
-# (per-CTA timeline stamps, read back with gemm_plan_trace).
-VARIANT_DEFINES = {"": [], "trace": ["-DGEMM_TRACE"]}
+# (per-CTA timeline stamps, read back with gemm_plan_trace); "debug" adds
+# -DGEMM_DEBUG (consistency checks of tile coordinates, ring stage and phase,
+# k-block ranges and store boxes inside the kernel, reported as
+# GEMM_ERR_INTERNAL through gemm_plan_status).
+VARIANT_DEFINES = {"": [], "trace": ["-DGEMM_TRACE"], "debug": ["-DGEMM_DEBUG"]}
 
 
 def lib_path(variant: str = "") -> str:
@@ -110,4 +113,4 @@ def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                variant="trace" if "--trace" in sys.argv else ""))
+                variant="trace" if "--trace" in sys.argv else "debug" if "--debug" in sys.argv else ""))

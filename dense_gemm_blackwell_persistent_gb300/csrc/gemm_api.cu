@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -144,6 +145,12 @@ struct gemm_plan {
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
     int* d_status = nullptr;      // 4 ints, see Params::status
+    // Clock log (GEMM_OPT_CLOCK_LOG): a ring of clock_cap records of two
+    // 64-bit words (SM cycles, ns of CTA 0's lifetime), one per launch;
+    // clock_next counts the launches since the log was last read.
+    unsigned long long* d_clock = nullptr;
+    int64_t clock_cap = 0;
+    std::atomic<int64_t> clock_next{0};
     // The last run's launch shape, for reports.  Every run writes it, so
     // runs from several host threads at once take rec_mu for it.
     std::mutex rec_mu;
@@ -190,6 +197,32 @@ int validate(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
     return GEMM_OK;
 }
 
+// The operands of a run on `device`: that device must be current, and A, B
+// (when K > 0) and C must be device memory of that device.  Host memory
+// (pinned or not), managed memory and another GPU's memory are refused
+// before anything is encoded or launched: the tensor maps would otherwise
+// hand the TMA unit addresses it must not read through, and the 4-CTA unit's
+// multicast copies are meant for this GPU's own memory only.  Host buffers
+// go through gemm_plan_run_host.
+int check_operands(int device, const void* A, const void* B, const void* C, int64_t K) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (cur != device) return GEMM_ERR_INVALID_ARG;
+    const void* ptrs[3] = {C, A, B};
+    for (int i = 0; i < (K > 0 ? 3 : 1); ++i) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_INVALID_ARG;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != device) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
 // CTAs the device keeps resident with the largest unit size that fits
 // best; the plan's per-CTA buffers (stream-K workspace, trace) are sized
 // for this many.
@@ -205,6 +238,8 @@ constexpr bool same_widths(int i = 0) {
 }
 static_assert(kLaunchTileWidths == kNumTileWidths && same_widths(), "tile widths: launch choice and kernel table agree");
 static_assert(kLaunchRowsPerCta == kRowsPerCta && kLaunchMnBox == kMnBoxElems, "launch choice and kernel agree");
+static_assert(kErrTimeout == GEMM_ERR_TIMEOUT && kErrCuda == GEMM_ERR_CUDA && kErrInternal == GEMM_ERR_INTERNAL,
+              "device-side status codes are the header's");
 
 int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype, int layout) {
     return launch_unit_ctas(plan->pair, plan->multicast, plan->visible_devices, K, elem_bytes(in_dtype), layout);
@@ -286,6 +321,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.stall_test = plan->stall_test;
     p.trace = plan->d_trace;
     p.trace_ctas = max_resident_ctas(plan);
+    p.clock_rec = nullptr;
 
     CUtensorMap tmA, tmB, tmC;
     // K-major operand: rows of K, box {one 128-byte row of K, rows}.  MN-major
@@ -335,6 +371,10 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (plan->d_clock != nullptr) {
+        const int64_t slot = plan->clock_next.fetch_add(1) % plan->clock_cap;
+        p.clock_rec = plan->d_clock + 2 * slot;
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, ki.fn, tmA, tmB, tmC, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -508,6 +548,36 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
             plan->visible_devices = n;
             return GEMM_OK;
         }
+        case GEMM_OPT_CLOCK_LOG: {
+            if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+            int prev = 0;
+            cudaGetDevice(&prev);
+            if (cudaSetDevice(plan->device) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            int rc = GEMM_OK;
+            if (plan->d_clock) {
+                cudaFree(plan->d_clock);   // waits for the device: no launch still writes it
+                plan->d_clock = nullptr;
+            }
+            plan->clock_cap = 0;
+            plan->clock_next = 0;
+            if (value > 0) {
+                const size_t bytes = (size_t)value * 2 * sizeof(unsigned long long);
+                if (cudaMalloc(&plan->d_clock, bytes) != cudaSuccess ||
+                    cudaMemset(plan->d_clock, 0, bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    if (plan->d_clock) cudaFree(plan->d_clock);
+                    plan->d_clock = nullptr;
+                    rc = GEMM_ERR_CUDA;
+                } else {
+                    plan->clock_cap = value;
+                }
+            }
+            cudaSetDevice(prev);
+            return rc;
+        }
         case GEMM_OPT_TILE_N: {
             if (value == 0) {
                 plan->tile_n = 0;
@@ -529,6 +599,8 @@ int gemm_plan_run(gemm_plan_t plan, const void* A, const void* B, void* C, int64
     if (!plan) return GEMM_ERR_INVALID_ARG;
     int rc = validate(A, B, C, M, N, K, dtype, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    rc = check_operands(plan->device, A, B, C, K);
+    if (rc != GEMM_OK) return rc;
     return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream));
 }
 
@@ -537,6 +609,8 @@ int gemm_plan_run_layout(gemm_plan_t plan, const void* A, const void* B, void* C
     if (!plan) return GEMM_ERR_INVALID_ARG;
     int rc = validate(A, B, C, M, N, K, dtype, out_dtype, layout);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    rc = check_operands(plan->device, A, B, C, K);
+    if (rc != GEMM_OK) return rc;
     return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream), layout);
 }
 
@@ -554,6 +628,8 @@ int gemm_plan_run_batched(gemm_plan_t plan, const void* A, const void* B, void* 
         if (stride_c < M * N || (stride_a != 0 && stride_a < M * K) || (stride_b != 0 && stride_b < N * K))
             return GEMM_ERR_INVALID_ARG;
     }
+    rc = check_operands(plan->device, A, B, C, K);
+    if (rc != GEMM_OK) return rc;
     Batch bt;
     bt.count = batch;
     bt.sa = stride_a;
@@ -577,6 +653,8 @@ int gemm_run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_
         if (dev >= 0 && dev < kMaxDevices && !g_plans[dev].empty()) plan = g_plans[dev].back();
     }
     if (!plan) return GEMM_ERR_NO_PLAN;
+    rc = check_operands(plan->device, A, B, C, K);
+    if (rc != GEMM_OK) return rc;
     return launch(plan, A, B, C, M, N, K, dtype, out_dtype, static_cast<cudaStream_t>(stream));
 }
 
@@ -605,6 +683,12 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
     if (!plan) return GEMM_ERR_INVALID_ARG;
     int rc = validate(A_host, B_host, C_host, M, N, K, dtype, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (cur != plan->device) return GEMM_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t bytes[3] = {(size_t)M * (size_t)K * elem_bytes(dtype), (size_t)N * (size_t)K * elem_bytes(dtype),
                              (size_t)M * (size_t)N * (size_t)elem_bytes(out_dtype)};
@@ -662,7 +746,7 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
                  cudaStreamWaitEvent(sX, plan->hev_a[c], 0) == cudaSuccess;
         if (ok) {
             rc = launch(plan, a_dev, plan->hbuf[1], c_dev, mc, N, K, dtype, out_dtype, sX);
-            if (rc != GEMM_OK) return rc;
+            ok = rc == GEMM_OK;
         }
         ok = ok && cudaEventRecord(plan->hev_c[c], sX) == cudaSuccess &&
              cudaStreamWaitEvent(sC, plan->hev_c[c], 0) == cudaSuccess &&
@@ -673,8 +757,13 @@ int gemm_plan_run_host(gemm_plan_t plan, const void* A_host, const void* B_host,
     ok = ok && cudaEventRecord(plan->hev_done, sC) == cudaSuccess &&
          cudaStreamWaitEvent(s, plan->hev_done, 0) == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
     if (!ok) {
+        // Copies queued before the failure may still read the caller's host
+        // buffers or write the plan's: the call is synchronous, so they end
+        // before it returns, whatever failed.
         cudaGetLastError();
-        return GEMM_ERR_CUDA;
+        for (int i = 0; i < 3; ++i) cudaStreamSynchronize(plan->hstream[i]);
+        cudaGetLastError();
+        return rc != GEMM_OK ? rc : GEMM_ERR_CUDA;
     }
     return GEMM_OK;
 }
@@ -723,6 +812,34 @@ int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
     return GEMM_OK;
 }
 
+int gemm_plan_clock_log(gemm_plan_t plan, uint64_t* host, int64_t capacity, int64_t* count) {
+    if (!plan || !count || capacity < 0 || (capacity > 0 && host == nullptr)) return GEMM_ERR_INVALID_ARG;
+    *count = 0;
+    if (plan->d_clock == nullptr) return GEMM_ERR_UNSUPPORTED;
+    const int64_t cap = plan->clock_cap;
+    std::vector<unsigned long long> ring((size_t)cap * 2);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (cudaSetDevice(plan->device) != cudaSuccess ||
+        cudaMemcpy(ring.data(), plan->d_clock, ring.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        cudaSetDevice(prev);
+        return GEMM_ERR_CUDA;
+    }
+    cudaSetDevice(prev);
+    const int64_t launched = plan->clock_next.exchange(0);
+    const int64_t kept = std::min(launched, cap), n = std::min(kept, capacity);
+    // the last n launches, oldest first: launch j went to slot j % cap
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t slot = (launched - n + i) % cap;
+        host[2 * i] = ring[(size_t)(2 * slot)];
+        host[2 * i + 1] = ring[(size_t)(2 * slot + 1)];
+    }
+    *count = n;
+    return GEMM_OK;
+}
+
 int gemm_plan_trace(gemm_plan_t plan, void* host, size_t bytes, int* ctas, int* slots) {
     if (!plan || !ctas || !slots) return GEMM_ERR_INVALID_ARG;
     *ctas = max_resident_ctas(plan);
@@ -755,6 +872,7 @@ int gemm_plan_destroy(gemm_plan_t plan) {
     if (plan->d_partials) cudaFree(plan->d_partials);
     if (plan->d_flags) cudaFree(plan->d_flags);
     if (plan->d_trace) cudaFree(plan->d_trace);
+    if (plan->d_clock) cudaFree(plan->d_clock);
     for (int i = 0; i < 3; ++i)
         if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);
     for (int i = 0; i < 3; ++i)
@@ -782,6 +900,7 @@ const char* gemm_strerror(int status) {
         case GEMM_ERR_NO_PLAN: return "no plan created for the current device";
         case GEMM_ERR_TIMEOUT: return "a bounded wait in the kernel expired";
         case GEMM_ERR_NO_DEVICE: return "no usable sm_103 device";
+        case GEMM_ERR_INTERNAL: return "an internal consistency check of a GEMM_DEBUG build failed";
         default: return "unknown status";
     }
 }
@@ -879,6 +998,8 @@ extern "C" int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M
     NoallocDevice* d = &g_noalloc[dev];
     std::call_once(d->once, noalloc_setup, d, dev);
     if (d->rc != GEMM_OK) return d->rc;
+    rc = check_operands(dev, A, B, C, K);
+    if (rc != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(d->state.d_status, 0, noalloc_scratch_bytes(M, N, K), s) != cudaSuccess) {
         cudaGetLastError();

@@ -143,6 +143,19 @@ constexpr int kErrTimeout = -7;
 constexpr int kRoleSmemBase = 9;  // status[1] for kErrCuda; status[3] = the base address
 constexpr int kRoleLayout = 10;   // status[1] for kErrCuda: an MN-major operand this tile cannot hold
 constexpr int kRoleClc = 11;      // status[1] of a timeout on the dynamic work list's ring (detail: item)
+constexpr int kErrInternal = -9;  // GEMM_DEBUG builds: a consistency check failed
+constexpr int kRoleDebug = 12;    // status[1] for kErrInternal; status[3] = which check (DebugCheck)
+
+// Consistency checks of GEMM_DEBUG builds (status[3] of a kErrInternal record).
+enum DebugCheck {
+    kChkWorkItem = 1,     // a work item's tile or k-block range outside the problem
+    kChkTileCoords = 2,   // tile coordinates (batch element, tile row, tile column) outside the tile grid
+    kChkOperandRows = 3,  // first A or B row of a load beyond the tile grid's rows
+    kChkRing = 4,         // ring stage or phase out of range
+    kChkKBlock = 5,       // k-block outside [0, k_blocks)
+    kChkAccumulator = 6,  // accumulator buffer or phase out of range
+    kChkStoreBox = 7,     // epilogue store box outside the tile grid
+};
 
 struct Params {
     // What decoding a work item reads comes first, so that it shares one
@@ -165,6 +178,10 @@ struct Params {
     int a_mn, b_mn;    // 1: A stored K×M / B stored K×N (MN-major in shared memory)
     unsigned long long* trace;  // GEMM_TRACE builds only: kTraceSlots words per CTA
     int trace_ctas;             // CTAs the trace buffer holds (CTAs with a higher index record nothing)
+    // Per-launch clock record, or null: CTA 0 writes the SM cycles and the
+    // %globaltimer nanoseconds between its entry and its exit (their ratio
+    // is the SM clock the launch ran at).
+    unsigned long long* clock_rec;
 };
 
 // fp32 partial of one epilogue warp: 32 rows × 256 columns, stored as
@@ -277,6 +294,24 @@ __device__ __forceinline__ void record_error(const Params& p, int role, int deta
     }
 }
 
+// GEMM_DEBUG builds: `cond` must hold; if not, record kErrInternal (role
+// kRoleDebug, detail `what`) and raise the CTA's abort flag, so that every
+// role leaves its loop without the access and the CTA tears down as after a
+// timeout.  Other builds: no code, always true.
+#ifdef GEMM_DEBUG
+__device__ __forceinline__ bool debug_check(bool cond, volatile uint32_t* abort_flag, const Params& p, int what) {
+    if (!cond) {
+        record_error(p, kRoleDebug, what, kErrInternal);
+        *abort_flag = 1;
+    }
+    return cond;
+}
+// A check taken by a whole warp: true only if it holds for every lane.
+#define GEMM_WARP_CHECK(cond, what) __all_sync(0xffffffffu, debug_check((cond), abort_flag, p, (what)))
+#else
+#define GEMM_WARP_CHECK(cond, what) true
+#endif
+
 // Wait for the phase of parity `parity` of `bar`, for at most p.wait_limit_ns.
 // Returns false (and raises the CTA's abort flag) if the bound expires or
 // another role of this CTA has already aborted.
@@ -357,6 +392,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         GEMM_TR_SET(kTrSmid, (unsigned long long)sm_id() + 1);
     }
 #endif
+    // Clock record: CTA 0's first thread stamps entry here and exit at the end.
+    const bool clock_owner = p.clock_rec != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+    unsigned long long clk_entry = 0, ns_entry = 0;
+    if (clock_owner) {
+        clk_entry = (unsigned long long)clock64();
+        ns_entry = global_timer_ns();
+    }
     const uint32_t base = smem_addr(smem_raw);
     uint8_t* smem = smem_raw;
     if (base & 1023u) {
@@ -459,6 +501,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         w = whole_tile(list_tile(cur.owner, cur.pos++), p.k_blocks);
         return 1;
     };
+#ifdef GEMM_DEBUG
+    auto item_ok = [&](const Work& w) {
+        return w.tile >= 0 && w.tile < p.num_tiles && w.kb_begin >= 0 && w.kb_begin < w.kb_end &&
+               w.kb_end <= p.k_blocks;
+    };
+    auto rows_ok = [&](int a_row, int b_row, int bt) {
+        return bt >= 0 && bt * p.tiles_per_batch < p.num_tiles && a_row >= 0 && a_row < p.tiles_m * C::kTileM &&
+               b_row >= 0 && b_row < p.tiles_n * kBN;
+    };
+#endif
 
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
@@ -552,11 +604,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 // the last item of a list: ask for the next list now
                 if (requester && cur.pos == cur.len && !(ok = request(cur.resp))) break;
+                if (!GEMM_WARP_CHECK(item_ok(w), kChkWorkItem)) {
+                    ok = false;
+                    break;
+                }
                 int a_row, b_row, bt;
                 operand_rows(w.tile, a_row, b_row, bt);
+                if (!GEMM_WARP_CHECK(rows_ok(a_row, b_row, bt), kChkOperandRows)) {
+                    ok = false;
+                    break;
+                }
                 const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;   // batch coordinates
                 if (j == 0 && lane == 0) GEMM_TR_CLK(5);
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                    if (!GEMM_WARP_CHECK(stage < (uint32_t)kStages && phase <= 1u, kChkRing) ||
+                        !GEMM_WARP_CHECK(kb >= 0 && kb < p.k_blocks, kChkKBlock)) {
+                        ok = false;
+                        break;
+                    }
                     const uint64_t tw = GEMM_TR_NOW();
                     if (!__all_sync(0xffffffffu,
                                     wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb))) {
@@ -649,6 +714,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 }
                 const uint32_t b = i & 1, aphase = (i >> 1) & 1;
+                if (!GEMM_WARP_CHECK(item_ok(w), kChkWorkItem) ||
+                    !GEMM_WARP_CHECK(b < 2u && aphase <= 1u && b * kAccStride + kBN <= (uint32_t)kTmemCols,
+                                     kChkAccumulator)) {
+                    ok = false;
+                    break;
+                }
                 const uint64_t ta = GEMM_TR_NOW();
                 if (!__all_sync(0xffffffffu, wait_bounded<true>(acce_bar(b), aphase ^ 1u, abort_flag, p, 2, i))) {
                     ok = false;
@@ -658,6 +729,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * kAccStride;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                    if (!GEMM_WARP_CHECK(stage < (uint32_t)kStages && phase <= 1u, kChkRing) ||
+                        !GEMM_WARP_CHECK(kb >= 0 && kb < p.k_blocks, kChkKBlock)) {
+                        ok = false;
+                        break;
+                    }
                     const uint64_t tf = GEMM_TR_NOW();
                     if (!__all_sync(0xffffffffu, wait_bounded<(kCluster > 1)>(full_bar(stage), phase, abort_flag, p, 3, kb))) {
                         ok = false;
@@ -767,10 +843,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (gn < 0) break;
             if (warp == 2 && lane == 0) GEMM_TR_ITEM(kTrEpiStart, i);
             tc_fence_after_sync();
+            if (!GEMM_WARP_CHECK(item_ok(w), kChkWorkItem)) break;
             int bt, mt, nt;
             tile_coords(p, w.tile, bt, mt, nt);
+            if (!GEMM_WARP_CHECK(bt >= 0 && bt * p.tiles_per_batch < p.num_tiles && mt >= 0 && mt < p.tiles_m &&
+                                     nt >= 0 && nt < p.tiles_n,
+                                 kChkTileCoords))
+                break;
             const int row0 = mt * C::kTileM + (int)crank * kRowsPerCta + quad * 32;
             const int col0 = nt * kBN;
+            if (!GEMM_WARP_CHECK(row0 + 32 <= p.tiles_m * C::kTileM && col0 + kBN <= p.tiles_n * kBN &&
+                                     b < 2u && aphase <= 1u,
+                                 kChkStoreBox))
+                break;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
             if (w.ncontrib == 1 && gn == 0) {
                 // The unit's last tile: nothing overlaps its epilogue, and its
@@ -935,6 +1020,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     if (threadIdx.x == 0) GEMM_TR(kTrExit);
     if (lane == 0 && warp <= 1) GEMM_TR_CLK_FLUSH();
+    if (clock_owner) {
+        const unsigned long long clk = (unsigned long long)clock64(), ns = global_timer_ns();
+        p.clock_rec[0] = clk - clk_entry;
+        p.clock_rec[1] = ns - ns_entry;
+    }
 }
 
 }  // namespace gb300

@@ -12,9 +12,14 @@
  *
  * Device.  Everything runs on one GB300 GPU.  A, B and C are device pointers
  * owned by the caller; the library never allocates, frees or retains them.
- * Work is enqueued asynchronously on the caller's stream (a cudaStream_t,
- * passed as void* so that this header needs no CUDA header); 0 means the
- * legacy default stream.
+ * Each run checks, before it encodes or launches anything, that the device
+ * it runs on (the plan's; for gemm_run_noalloc the current one) is current
+ * and that A, B (when K > 0) and C are device memory of that device
+ * (cudaPointerGetAttributes); host memory, managed memory and another
+ * GPU's memory return GEMM_ERR_INVALID_ARG.  Host buffers go through
+ * gemm_plan_run_host.  Work is enqueued asynchronously on the caller's
+ * stream (a cudaStream_t, passed as void* so that this header needs no CUDA
+ * header); 0 means the legacy default stream.
  *
  * Layout rules (checked on the host before anything is launched):
  *   - A, B, C 16-byte aligned;
@@ -66,7 +71,9 @@ typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2, GEMM_E4M3 = 3, GEMM_E5
 
 typedef enum {
     GEMM_OK = 0,
-    GEMM_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad dtype pair, bad option */
+    GEMM_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad dtype pair, bad option,
+                                    an operand that is not device memory of the run's
+                                    device, or that device not current                 */
     GEMM_ERR_UNSUPPORTED = -2,   /* shape/pitch TMA cannot address (see layout rules)       */
     GEMM_ERR_MISALIGNED = -3,    /* a pointer not 16-byte aligned                            */
     GEMM_ERR_CUDA = -4,          /* a CUDA runtime call failed (launch, attribute, copy);
@@ -75,7 +82,11 @@ typedef enum {
     GEMM_ERR_DRIVER = -5,        /* the driver's tensor-map encoder failed or is missing     */
     GEMM_ERR_NO_PLAN = -6,       /* gemm_run with no plan created for the current device     */
     GEMM_ERR_TIMEOUT = -7,       /* device side: a bounded wait expired (see gemm_plan_status) */
-    GEMM_ERR_NO_DEVICE = -8      /* no usable sm_103 device                                   */
+    GEMM_ERR_NO_DEVICE = -8,     /* no usable sm_103 device                                   */
+    GEMM_ERR_INTERNAL = -9       /* device side, GEMM_DEBUG builds only: a consistency check
+                                    (tile coordinates, ring stage or phase, k-block range,
+                                    store box) failed; the access was skipped and the kernel
+                                    ended early (see gemm_plan_status)                   */
 } gemm_status_t;
 
 typedef struct gemm_plan* gemm_plan_t;
@@ -107,7 +118,14 @@ typedef enum {
                                     along K when there are fewer than half as many
                                     tiles as units, where that is predicted to pay;
                                     runs that may overlap on the GPU then need
-                                    separate plans.  0 (default): whole tiles only     */
+                                    separate plans.  The unit finishing a split tile
+                                    waits for a flag the other unit raises, so every
+                                    unit of the launch must be resident at once: if
+                                    other work on the GPU keeps some units from
+                                    starting until the waiting ones end, the run ends
+                                    with GEMM_ERR_TIMEOUT (after the wait bound) and C
+                                    undefined, not with a result.  0 (default): whole
+                                    tiles only, no unit waits for another            */
     GEMM_OPT_MULTICAST = 6,      /* with CTA pairs: 1 = two pairs per 4-CTA cluster work
                                     on vertically adjacent tiles and share their B tile
                                     through TMA multicast (512×BN per cluster); 0 = one
@@ -144,6 +162,11 @@ typedef enum {
                                     rejects the output map, so runs on this plan
                                     return GEMM_ERR_DRIVER before any launch and
                                     leave C untouched; 0 (default) = off            */
+    GEMM_OPT_CLOCK_LOG = 12,     /* measurement: keep a record of the SM clock of the
+                                    last `value` launches (0..2^20; 0 = off, the
+                                    default), read by gemm_plan_clock_log.  Setting it
+                                    allocates (or frees) value × 16 bytes of device
+                                    memory and waits for the device                  */
     GEMM_OPT_VISIBLE_DEVICES = 11 /* GPUs the plan counts as visible to the process,
                                     1..1024 (0 = default: cudaGetDeviceCount at plan
                                     creation).  TMA multicast stays within one GPU's
@@ -233,6 +256,17 @@ int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);
 int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* tile_n, int* dp_waves,
                           int* sk_tiles);
 
+/* Clock log of the plan's launches since the last call (GEMM_OPT_CLOCK_LOG
+ * must be set; GEMM_ERR_UNSUPPORTED otherwise): for each of the most recent
+ * min(launches, option value, capacity) launches, oldest first, two words
+ * go to host[2i] and host[2i+1]: the SM cycles (clock64) and the
+ * nanoseconds (%globaltimer) between the entry and the exit of the launch's
+ * first CTA.  cycles ÷ ns × 1000 is the SM clock in MHz the launch ran at.
+ * *count receives the number of records copied; the log is then empty.
+ * Launches that filled K = 0 or M/N = 0 problems record nothing.
+ * Synchronises the device.  host: room for 2 × capacity words. */
+int gemm_plan_clock_log(gemm_plan_t plan, uint64_t* host, int64_t capacity, int64_t* count);
+
 /* Timeline of the last runs, for builds compiled with GEMM_TRACE (other
  * builds return GEMM_ERR_UNSUPPORTED after filling *ctas and *slots).  Copies
  * *ctas × *slots 64-bit words to `host` (at least that many bytes) and
@@ -264,15 +298,18 @@ int gemm_plan_destroy(gemm_plan_t plan);
  *     first call before any stream capture.
  *   - Each call clears the status record on `stream` before launching.
  *     Every call on a device shares the array, so calls that overlap on the
- *     GPU (unordered streams) race on it.  Device-side timeouts are not
- *     reported by this entry point; gemm_plan_status() covers the plan path.
+ *     GPU (unordered streams) race on it.  This entry point never reads the
+ *     record back: every device-side error -- a wait that outlived its bound
+ *     (GEMM_ERR_TIMEOUT) and the kernel's own set-up checks (a shared-memory
+ *     window not 1 KB aligned, GEMM_ERR_CUDA) -- goes unreported, and C is
+ *     then undefined although the call returned GEMM_OK.  Callers that need
+ *     those errors use the plan path and gemm_plan_status().
  *   - A scratch requirement beyond the array's 256 bytes is rejected with
  *     GEMM_ERR_UNSUPPORTED (the kernel needs 16 bytes whatever M, N, K).
  * The pages have no counterpart: this is a library integration entry point. */
 int gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                      int dtype, int out_dtype, void* stream);
 
-/* Static text for a status code. */
 /* Tensor-core issue-rate probe (a measurement, not part of a product):
  * on the current device every SM holds one CTA (cta_pair = 1) or one CTA of
  * a pair (cta_pair = 2), and one thread per CTA (pair) issues
@@ -300,6 +337,7 @@ int gemm_probe_mma_rate(int dtype, int cta_pair, int64_t mmas_per_sm, double* fl
 int gemm_probe_mma_rate_n(int dtype, int cta_pair, int tile_n, int64_t mmas_per_sm, double* flop_per_clk_per_sm,
                           double* tflops, double* sm_mhz);
 
+/* Static text for a status code. */
 const char* gemm_strerror(int status);
 
 #ifdef __cplusplus

@@ -14,7 +14,8 @@ What pins what:
     torch's float8 types.
   * the product: a hand-worked example (tests/golden), closed forms (identity,
     all-ones, rank-1 outer products with distinct factors), exact rational
-    brute force on every shape up to 4×4×4, numpy float64 matmul within the
+    brute force on every shape up to 8×8×8 for the 16-bit formats (up to
+    4×4×4 for the 8-bit ones), numpy float64 matmul within the
     float64 summation bound, symmetry C(B,A) = C(A,B)ᵀ, power-of-two
     scaling, IEEE special values, and empty sizes; for fp8 inputs, exact
     rational brute force, agreement with the bf16 path on values both

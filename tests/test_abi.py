@@ -86,7 +86,10 @@ def test_host_validation_without_gpu(lib):
     assert rs("gemm_probe_mma_rate", 0, 2, 6, None, None, None) == lib.GEMM_ERR_INVALID_ARG         # not whole k-blocks
     for n in (0, 8, 100, 272):                                                                      # not an MMA width
         assert rs("gemm_probe_mma_rate_n", 0, 2, n, 1 << 12, None, None, None) == lib.GEMM_ERR_INVALID_ARG
-    for code in range(-8, 1):
+    # the clock log checks its arguments before touching the device
+    n = ctypes.c_int64(0)
+    assert rs("gemm_plan_clock_log", None, None, 0, ctypes.byref(n)) == lib.GEMM_ERR_INVALID_ARG
+    for code in range(-9, 1):
         assert lib.gemm_strerror(code) != "unknown status"
 
 

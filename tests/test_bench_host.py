@@ -89,3 +89,41 @@ def test_clock_summary_from_nvidia_smi_lines():
         "0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"])
     assert throttled["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
     assert bench.summarise_clocks([])["sm_mhz"] is None
+
+
+def test_roofline_bound_is_the_slower_term():
+    """The bound is whichever is slower: the FLOPs at the measured tensor peak
+    or the compulsory bytes at the measured copy bandwidth; achieved and peak
+    are then in that bound's unit, and the fractions at the maximum and at
+    the launches' own SM clock follow from the issue-rate probe."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "sm_max_mhz": 2000.0}
+    probe = {"flop_per_clk_per_sm": 8192.0}
+    w = wl.WORKLOADS["gemm_4096_bf16"]
+    ms = w.flops / 1.5e15 * 1e3                       # 1500 TFLOP/s
+    r = bench.roofline(w, 1500.0, ms, peaks, "measured", probe, 152, {"sm_mhz_median": 1800.0})
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - 0.75) < 1e-12
+    assert abs(r["peak_clock_tflops"] - 8192 * 152 * 2000 / 1e6) < 1e-6
+    assert abs(r["frac_kernel_clock"] - 1500.0 / (8192 * 152 * 1800 / 1e6)) < 1e-12
+    # 256^3: 0.5 MB of compulsory bytes outweigh 34 MFLOP at this peak
+    w1 = wl.WORKLOADS["gemm_256_f32out"]
+    r1 = bench.roofline(w1, 4.0, w1.flops / 4e12 * 1e3, peaks, "measured", None, 152, None)
+    assert r1["bound"] == "hbm" and r1["unit"] == "GB/s"
+    assert abs(r1["achieved"] - w1.compulsory_bytes / (w1.flops / 4e12) / 1e9) < 1e-6
+    assert "frac_peak_clock" not in r1
+    # 8-bit operands: twice the bf16 peak
+    w8 = wl.WORKLOADS["gemm_4096_e4m3"]
+    assert bench.roofline(w8, 3000.0, 1.0, peaks, "measured", None, 152, None)["peak"] == 4000.0
+
+
+def test_kernel_clock_summary():
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = [(1800 * 50, 50_000), (1900 * 60, 60_000), (1700 * 70, 70_000), (5, 0)]
+    k = bench.kernel_clock(rec)
+    assert k["launches"] == 3 and abs(k["sm_mhz_median"] - 1800.0) < 1e-9
+    assert abs(k["sm_mhz_min"] - 1700.0) < 1e-9 and abs(k["sm_mhz_max"] - 1900.0) < 1e-9
+    assert bench.kernel_clock([]) is None

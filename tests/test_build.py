@@ -19,9 +19,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "dense_gemm_blackwell_persistent_gb300", "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 
-# (CTAs per unit, output type, operand width, padded MN-major B): pairs with bf16 C (the
-# benchmark's kernel), the 4-CTA multicast unit with fp32 C, 8-bit operands, the padded form
-CASES = [(2, 0, 0, 0), (4, 2, 0, 0), (2, 0, 1, 0), (1, 1, 0, 1)]
+# (CTAs per unit, output type, operand width, padded MN-major B, extra defines): pairs with bf16
+# C (the benchmark's kernel), the 4-CTA multicast unit with fp32 C, 8-bit operands, the padded
+# form, and the benchmark's kernel in the GEMM_DEBUG build (its checks must not spill either)
+CASES = [(2, 0, 0, 0, ""), (4, 2, 0, 0, ""), (2, 0, 1, 0, ""), (1, 1, 0, 1, ""), (2, 0, 0, 0, "-DGEMM_DEBUG")]
 
 
 def _nvcc():
@@ -32,11 +33,12 @@ def _nvcc():
 
 
 def _ptxas_report(case, tmp):
-    cluster, out, inp, pad = case
+    cluster, out, inp, pad, extra = case
     cmd = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "--expt-relaxed-constexpr",
            "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC, f"-DGEMM_INST_CLUSTER={cluster}", f"-DGEMM_INST_OUT={out}",
-           f"-DGEMM_INST_IN={inp}", f"-DGEMM_INST_BMN={pad}", "-c", os.path.join(CSRC, "kernels_inst.cu"),
-           "-o", os.path.join(tmp, "k_{}_{}_{}_{}.o".format(*case))]
+           f"-DGEMM_INST_IN={inp}", f"-DGEMM_INST_BMN={pad}", *([extra] if extra else []), "-c",
+           os.path.join(CSRC, "kernels_inst.cu"),
+           "-o", os.path.join(tmp, "k_{}_{}_{}_{}{}.o".format(*case[:4], "_dbg" if extra else ""))]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr[-2000:]
     return res.stdout + res.stderr

@@ -78,3 +78,20 @@ def test_planted_mistake_is_caught(tmp_path, desc, old, new):
         except Exception as e:  # a crash in a mutant also counts as caught
             failed.append(f"{pin.__name__}:{type(e).__name__}")
     assert failed, f"no pin caught the planted mistake: {desc}"
+
+
+@pytest.mark.parametrize("name,shape", [("gemm_256_f32out", None), ("gemm_ragged_4000x3000x5000", (1000, 760, 1256)),
+                                        ("gemm_1024x4096x4096_f16", (264, 392, 1024))])
+def test_torch_fp32_second_opinion(real_oracle, name, shape):
+    """An untrusted second opinion: torch's CPU matmul in fp32 on the inputs
+    widened exactly to fp32 agrees with the oracle within the fp32
+    accumulation bound |C - C_ref| <= 1e-5 * S used for the kernel (the
+    256³ workload, and the ragged and f16 workloads' distributions at sizes
+    that still span several tiles)."""
+    import torch
+    import workloads as wl
+    w = wl.WORKLOADS[name]
+    A, B = wl.make_inputs(w) if shape is None else wl.make_inputs(w, *shape, seed=w.seed + 100)
+    C_ref, S = real_oracle.gemm(wl.as_bits(A), wl.as_bits(B), w.dtype)
+    C_t = torch.matmul(A.float(), B.float().t()).double().numpy()
+    assert np.all(np.abs(C_t - C_ref) <= 1e-5 * S), float(np.max(np.abs(C_t - C_ref) / S))
