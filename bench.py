@@ -518,9 +518,32 @@ def sustained_line(torch, g, args, name, seconds, stream, local):
     finally:
         g.gemm_plan_destroy(plan)
     ms = ev0.elapsed_time(ev1)
-    return {"value": w.flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n, "seconds": ms / 1e3,
+    line = {"value": w.flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n, "seconds": ms / 1e3,
             "kernel_clock": kernel_clock(records), "clocks": smi,
             "how": "back-to-back launches, operands resident (no flush), events around the whole loop"}
+    if not args.no_cublas:
+        # cuBLAS the same way, right after: same inputs, as many launches
+        call, how = cublas_call(torch, w, A, B, wl.TORCH_DTYPES[w.out_dtype])
+        try:
+            for _ in range(10):
+                call()
+            torch.cuda.synchronize()
+            sampler = ClockSampler(local)
+            sampler.start()
+            time.sleep(0.25)
+            ev0.record(stream)
+            for _ in range(n):
+                call()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            smi_ref = sampler.stop()
+            ms_ref = ev0.elapsed_time(ev1)
+            line["cublas_reference"] = {"value": w.flops * n / (ms_ref / 1e3) / 1e12, "unit": "TFLOP/s",
+                                        "launches": n, "seconds": ms_ref / 1e3, "clocks": smi_ref,
+                                        "how": f"{how}, back to back right after, same inputs"}
+        except (RuntimeError, NotImplementedError, TypeError) as e:
+            line["cublas_reference"] = {"unavailable": f"{how}: " + str(e).splitlines()[0][:200]}
+    return line
 
 
 def main():

@@ -312,16 +312,37 @@ __device__ __forceinline__ bool debug_check(bool cond, volatile uint32_t* abort_
 #define GEMM_WARP_CHECK(cond, what) true
 #endif
 
+// Suspend-time hints of the waits (ns; 0 = the hardware's own limit): the
+// epilogue warps wait for an accumulator for a whole tile's K loop, the
+// producer and MMA warps for ring slots a few hundred cycles at a time.
+#ifndef GEMM_EPI_WAIT_HINT_NS
+#define GEMM_EPI_WAIT_HINT_NS 20000
+#endif
+#ifndef GEMM_RING_WAIT_HINT_NS
+#define GEMM_RING_WAIT_HINT_NS 0
+#endif
+constexpr uint32_t kEpiWaitHintNs = GEMM_EPI_WAIT_HINT_NS;
+constexpr uint32_t kRingWaitHintNs = GEMM_RING_WAIT_HINT_NS;
+
+template <bool kClusterScope, uint32_t kHintNs>
+__device__ __forceinline__ bool try_wait_once(uint32_t bar, uint32_t parity) {
+    if constexpr (kHintNs == 0)
+        return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    else
+        return kClusterScope ? mbar_try_wait_cluster_hint(bar, parity, kHintNs)
+                             : mbar_try_wait_hint(bar, parity, kHintNs);
+}
+
 // Wait for the phase of parity `parity` of `bar`, for at most p.wait_limit_ns.
 // Returns false (and raises the CTA's abort flag) if the bound expires or
 // another role of this CTA has already aborted.
-template <bool kClusterScope>
+template <bool kClusterScope, uint32_t kHintNs = 0>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              const Params& p, int role, int detail) {
-    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (try_wait_once<kClusterScope, kHintNs>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (try_wait_once<kClusterScope, kHintNs>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > p.wait_limit_ns) {
             record_error(p, role, detail);
@@ -624,7 +645,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                     const uint64_t tw = GEMM_TR_NOW();
                     if (!__all_sync(0xffffffffu,
-                                    wait_bounded<(kCluster > 1)>(empty_bar(stage), phase ^ 1u, abort_flag, p, 0, kb))) {
+                                    wait_bounded<(kCluster > 1), kRingWaitHintNs>(empty_bar(stage), phase ^ 1u,
+                                                                                  abort_flag, p, 0, kb))) {
                         ok = false;
                         break;
                     }
@@ -735,7 +757,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     const uint64_t tf = GEMM_TR_NOW();
-                    if (!__all_sync(0xffffffffu, wait_bounded<(kCluster > 1)>(full_bar(stage), phase, abort_flag, p, 3, kb))) {
+                    if (!__all_sync(0xffffffffu, wait_bounded<(kCluster > 1), kRingWaitHintNs>(full_bar(stage), phase,
+                                                                                              abort_flag, p, 3, kb))) {
                         ok = false;
                         break;
                     }
@@ -835,7 +858,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int g = get_work(cur, w), gn = 0;
         for (int i = 0; g > 0; ++i) {
             const uint32_t b = i & 1, aphase = (i >> 1) & 1;
-            const bool got = wait_bounded<false>(accf_bar(b), aphase, abort_flag, p, 5, i);
+            const bool got = wait_bounded<false, kEpiWaitHintNs>(accf_bar(b), aphase, abort_flag, p, 5, i);
             if (!__all_sync(0xffffffffu, got)) break;
             // The next item now: whether this tile is the unit's last decides
             // how it is stored.
