@@ -289,13 +289,20 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.tiles_n = (int)((N + bn - 1) / bn);
     const int64_t kbe = kblock_elems(dtype);
     p.k_blocks = (int)((K + kbe - 1) / kbe);
-    p.tiles_per_batch = p.tiles_m * p.tiles_n;
-    if ((int64_t)p.tiles_per_batch * batch.count >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    // the tile space (batch elements × tiles) must fit the kernel's 32-bit tile indices
+    const int64_t tiles_per_batch = (int64_t)p.tiles_m * p.tiles_n;
+    if (tiles_per_batch >= (int64_t(1) << 31) || tiles_per_batch * batch.count >= (int64_t(1) << 31))
+        return GEMM_ERR_UNSUPPORTED;
+    p.tiles_per_batch = (int)tiles_per_batch;
     p.num_tiles = (int)(p.tiles_per_batch * batch.count);
     p.a_batched = batch.count > 1 && batch.sa != 0;
     p.b_batched = batch.count > 1 && batch.sb != 0;
     p.group_m = plan->group_m > 0 ? plan->group_m : 8;
     p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+    p.fd_batch = make_fastdiv((uint32_t)p.tiles_per_batch);
+    p.fd_group = make_fastdiv((uint32_t)(p.group_m * p.tiles_n));
+    p.fd_gm = make_fastdiv((uint32_t)p.group_m);
+    p.fd_gm_last = make_fastdiv((uint32_t)(p.tiles_m % p.group_m != 0 ? p.tiles_m % p.group_m : p.group_m));
     p.idesc = make_idesc(dtype, kRowsPerCta * pair, bn, layout);   // one MMA covers a pair's 256 rows
     p.a_mn = (layout & GEMM_A_MN_MAJOR) ? 1 : 0;
     p.b_mn = (layout & GEMM_B_MN_MAJOR) ? 1 : 0;

@@ -161,6 +161,11 @@ struct Params {
     // What decoding a work item reads comes first, so that it shares one
     // constant-cache line.
     Schedule sched;    // whole-tile waves + stream-K part
+    // Divisors of the tile decode as multiply-shift dividers: tiles per
+    // batch element, tiles per raster group (group_m * tiles_n), the group
+    // height, and the height of the last group (tiles_m mod group_m, or
+    // group_m when that is 0).
+    FastDiv fd_batch, fd_group, fd_gm, fd_gm_last;
     // Dynamic work list (cluster launch control): 1 = on.  Cluster c < dyn_units
     // owns tiles c, c + dyn_units, ... (dyn_waves of them); cluster c >=
     // dyn_units owns tile dyn_units * dyn_waves + (c - dyn_units).
@@ -275,15 +280,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 // within it, groups of `group_m` tile rows are walked column by column, so
 // the tiles in flight at once share rows of A and columns of Bᵀ in L2.
 __device__ __forceinline__ void tile_coords(const Params& p, int t, int& bt, int& mt, int& nt) {
-    bt = t / p.tiles_per_batch;
+    bt = (int)fast_div(p.fd_batch, (uint32_t)t);
     t -= bt * p.tiles_per_batch;
-    const int per_group = p.group_m * p.tiles_n;
-    const int g = t / per_group;
+    const int g = (int)fast_div(p.fd_group, (uint32_t)t);
     const int first_m = g * p.group_m;
-    const int gsize = min(p.tiles_m - first_m, p.group_m);
-    const int r = t - g * per_group;
-    mt = first_m + r % gsize;
-    nt = r / gsize;
+    const int r = t - g * (int)p.fd_group.d;
+    // the group's height: group_m, or fewer in the last group
+    const FastDiv& gs = first_m + p.group_m > p.tiles_m ? p.fd_gm_last : p.fd_gm;
+    const int q = (int)fast_div(gs, (uint32_t)r);
+    mt = first_m + (r - q * (int)gs.d);
+    nt = q;
 }
 
 __device__ __forceinline__ void record_error(const Params& p, int role, int detail, int code = kErrTimeout) {
@@ -533,6 +539,61 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     };
 #endif
 
+    // The unit's first work item, without waiting: a static list's first
+    // item, or the first tile of the unit's own dynamic list (every list
+    // has one).  The same item get_work() returns first.
+    auto first_item = [&](Work& w) -> bool {
+        if (!dyn) {
+            if (nwork <= 0) return false;
+            w = work_item(p.sched, pair_id, 0);
+        } else {
+            w = whole_tile(list_tile(pair_id, 0), p.k_blocks);
+        }
+        return true;
+    };
+    // The first k-blocks of the first item are loaded by epilogue warp 2 at
+    // start-up (see below): as many as the ring holds.
+    auto preissued = [&](const Work& w) { return min(kStages, w.kb_end - w.kb_begin); };
+
+    // Loads of k-block kb of a work item into ring slot `stage`, by one lane:
+    // the pair leader announces the pair's bytes on its full barrier; then
+    // this CTA's A rows and its share of the tile's B rows (in a 4-CTA unit a
+    // quarter, written to this CTA and to the same-rank CTA of the other
+    // pair).  In a pair the copies complete on the leader's barrier.
+    auto issue_loads = [&](int kb, uint32_t stage, int a_row, int b_row, int za, int zb) {
+        const uint32_t fb = full_bar(stage);
+        const uint32_t a_dst = base + stage * kStageBytesA;
+        const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
+        if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
+        const uint32_t fb_leader = kCluster > 1 ? map_shared_rank(fb, leader) : fb;
+        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
+        auto copy_a = [&](uint32_t dst, int x, int y) {
+            if constexpr (kCluster > 1) tma_load_3d_pair(dst, &tmA, fb_leader, x, y, za);
+            else tma_load_3d(dst, &tmA, fb, x, y, za);
+        };
+        auto copy_b = [&](uint32_t dst, int x, int y) {
+            if constexpr (kCluster == 4)
+                tma_load_3d_pair_multicast(dst, &tmB, fb_leader, mask, x, y, zb);
+            else if constexpr (kCluster == 2) tma_load_3d_pair(dst, &tmB, fb_leader, x, y, zb);
+            else tma_load_3d(dst, &tmB, fb, x, y, zb);
+        };
+        const int kx = kb * C::kBlockKElems;
+        const uint32_t b_q = b_dst + pidx * C::kLoadBytesB;
+        // K-major: one box {one 128-byte row of K, rows} at (k, row).
+        // MN-major: boxes {64 elements, 64 K rows} at (row, k).
+        if (p.a_mn) {
+            for (int h = 0; h < kRowsPerCta / kMnBoxElems; ++h)
+                copy_a(a_dst + h * kMnBoxBytes, a_row + h * kMnBoxElems, kx);
+        } else {
+            copy_a(a_dst, kx, a_row);
+        }
+        if (p.b_mn) {
+            for (int h = 0; h < C::kBoxesB; ++h) copy_b(b_q + h * kMnBoxBytes, b_row + h * kMnBoxElems, kx);
+        } else {
+            copy_b(b_q, kx, b_row);
+        }
+    };
+
     // ---- set-up: barriers, TMEM, tensor-map prefetch
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -563,8 +624,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // arrives on it before allocating TMEM and waits after, so the producer's
     // first loads do not wait for the allocation; the TMEM address reaches
     // the epilogue warps through a named barrier of warps 1-5.
+    // Epilogue warp 2, idle until the first accumulator is full, decodes the
+    // first work item while the barriers are set up and, once they are
+    // visible, issues that item's first ring-full of loads (the producer
+    // warp starts after them).  Each warp fetches its instructions on its
+    // own, so after an L2 flush the cold code of the decode and of the
+    // first issue is fetched while warp 0 initialises the barriers instead
+    // of after it.
+    Work w_first;
+    int pre_rows[3] = {0, 0, 0};   // a_row, b_row, batch element of the first item
+    bool pre_ok = false;
     if constexpr (kCluster > 1) cluster_arrive();
-    else __syncthreads();
+    if (warp == 2) {
+        pre_ok = first_item(w_first);
+        if (pre_ok) operand_rows(w_first.tile, pre_rows[0], pre_rows[1], pre_rows[2]);
+        if (lane == 0) GEMM_TR_SET(kTrClkPro + 5, (unsigned long long)clock64());
+    }
+    if constexpr (kCluster == 1) __syncthreads();
     if (threadIdx.x == 0) GEMM_TR_CLK(3);
     if (warp == 1) {
         tmem_alloc<kPair>(smem_addr(tmem_holder), kTmemCols);
@@ -572,6 +648,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     if constexpr (kCluster > 1) cluster_wait();
     if (threadIdx.x == 0) GEMM_TR_CLK(4);
+    if (warp == 2 && pre_ok) {
+#ifdef GEMM_DEBUG
+        pre_ok = GEMM_WARP_CHECK(item_ok(w_first) && rows_ok(pre_rows[0], pre_rows[1], pre_rows[2]), kChkOperandRows);
+#endif
+        if (lane == 0) GEMM_TR_SET(kTrClkPro + 6, (unsigned long long)clock64());
+        if (pre_ok && elect_one_sync()) {
+            const int za = p.a_batched ? pre_rows[2] : 0, zb = p.b_batched ? pre_rows[2] : 0;
+            const int n = preissued(w_first);
+            for (int i = 0; i < n; ++i) issue_loads(w_first.kb_begin + i, (uint32_t)i, pre_rows[0], pre_rows[1], za, zb);
+            GEMM_TR_SET(kTrClkPro + 7, (unsigned long long)clock64());
+        }
+        __syncwarp();
+    }
     uint32_t tmem_base = 0;
     if (warp >= 1) {
         tc_fence_before_sync();
@@ -636,8 +725,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 }
                 const int za = p.a_batched ? bt : 0, zb = p.b_batched ? bt : 0;   // batch coordinates
-                if (j == 0 && lane == 0) GEMM_TR_CLK(5);
-                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                int kb0 = w.kb_begin;
+                if (j == 0) {
+                    // epilogue warp 2 has issued the first item's first slots
+                    const int n = preissued(w);
+                    kb0 += n;
+                    stage = n == kStages ? 0u : (uint32_t)n;
+                    phase = n == kStages ? 1u : 0u;
+                }
+                for (int kb = kb0; kb < w.kb_end; ++kb) {
                     if (!GEMM_WARP_CHECK(stage < (uint32_t)kStages && phase <= 1u, kChkRing) ||
                         !GEMM_WARP_CHECK(kb >= 0 && kb < p.k_blocks, kChkKBlock)) {
                         ok = false;
@@ -651,46 +747,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     empty_wait_ns += GEMM_TR_NOW() - tw;
-                    if (j == 0 && kb == w.kb_begin && lane == 0) GEMM_TR_CLK(6);
-                    const uint32_t fb = full_bar(stage);
-                    const uint32_t a_dst = base + stage * kStageBytesA;
-                    const uint32_t b_dst = base + C::kOffB + stage * C::kStageBytesB;
-                    if (issuer) {
-                        if (rank == 0) mbar_arrive_expect_tx(fb, C::kTxBytes);
-                        // Own A rows; B: this CTA's share of the tile's B rows (in a
-                        // 4-CTA unit a quarter, written to this CTA and to the
-                        // same-rank CTA of the other pair).  In a pair the copies
-                        // complete on the leader's barrier.
-                        const uint32_t fb_leader = kCluster > 1 ? map_shared_rank(fb, leader) : fb;
-                        const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank + 2)));
-                        auto copy_a = [&](uint32_t dst, int x, int y) {
-                            if constexpr (kCluster > 1) tma_load_3d_pair(dst, &tmA, fb_leader, x, y, za);
-                            else tma_load_3d(dst, &tmA, fb, x, y, za);
-                        };
-                        auto copy_b = [&](uint32_t dst, int x, int y) {
-                            if constexpr (kCluster == 4)
-                                tma_load_3d_pair_multicast(dst, &tmB, fb_leader, mask, x, y, zb);
-                            else if constexpr (kCluster == 2) tma_load_3d_pair(dst, &tmB, fb_leader, x, y, zb);
-                            else tma_load_3d(dst, &tmB, fb, x, y, zb);
-                        };
-                        const int kx = kb * C::kBlockKElems;
-                        const uint32_t b_q = b_dst + pidx * C::kLoadBytesB;
-                        // K-major: one box {one 128-byte row of K, rows} at (k, row).
-                        // MN-major: boxes {64 elements, 64 K rows} at (row, k).
-                        if (p.a_mn) {
-                            for (int h = 0; h < kRowsPerCta / kMnBoxElems; ++h)
-                                copy_a(a_dst + h * kMnBoxBytes, a_row + h * kMnBoxElems, kx);
-                        } else {
-                            copy_a(a_dst, kx, a_row);
-                        }
-                        if (p.b_mn) {
-                            for (int h = 0; h < C::kBoxesB; ++h)
-                                copy_b(b_q + h * kMnBoxBytes, b_row + h * kMnBoxElems, kx);
-                        } else {
-                            copy_b(b_q, kx, b_row);
-                        }
-                        if (j == 0 && kb == w.kb_begin) GEMM_TR_CLK(7);
-                    }
+                    if (issuer) issue_loads(kb, stage, a_row, b_row, za, zb);
                     __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }

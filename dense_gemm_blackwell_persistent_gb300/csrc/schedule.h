@@ -47,6 +47,52 @@
 
 namespace gb300 {
 
+// Division by a divisor fixed for the whole launch, as a multiply and a
+// shift (T. Granlund and P. L. Montgomery, "Division by Invariant Integers
+// using Multiplication", PLDI 1994): for 1 <= d < 2^31 and 0 <= x < 2^31,
+// with l = ceil(log2 d) and p = 31 + l, m = ceil(2^p / d) < 2^32 and
+// x / d = floor(x * m / 2^p).  Why it is exact: m * d = 2^p + e with
+// 0 <= e < d, so x * m / 2^p = x / d + x * e / (d * 2^p), and the second term
+// is below 2^31 / 2^p = 2^-l <= 1 / d, too little to reach the next integer
+// from x / d, whose fraction is at most (d - 1) / d.  The host builds it once
+// per launch; the kernel's tile decode then needs no division instructions.
+// d == 1 is a plain copy (p - 32 would be negative).
+struct FastDiv {
+    uint32_t d;     // the divisor
+    uint32_t mul;   // m (unused when d == 1)
+    uint32_t shr;   // p - 32
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.mul = 0;
+    f.shr = 0;
+    if (d > 1) {
+        uint32_t l = 0;
+        while ((uint64_t(1) << l) < d) ++l;   // ceil(log2 d)
+        const uint32_t p = 31 + l;
+        f.mul = (uint32_t)(((uint64_t(1) << p) + d - 1) / d);
+        f.shr = p - 32;
+    }
+    return f;
+}
+
+#if defined(__CUDACC__)
+__host__ __device__ __forceinline__ uint32_t mul_hi_u32(uint32_t a, uint32_t b) {
+#if defined(__CUDA_ARCH__)
+    return __umulhi(a, b);
+#else
+    return (uint32_t)(((uint64_t)a * b) >> 32);
+#endif
+}
+#else
+inline uint32_t mul_hi_u32(uint32_t a, uint32_t b) { return (uint32_t)(((uint64_t)a * b) >> 32); }
+#endif
+
+// x / f.d for 0 <= x < 2^31.
+GB300_HD uint32_t fast_div(const FastDiv& f, uint32_t x) { return f.d == 1 ? x : mul_hi_u32(x, f.mul) >> f.shr; }
+
 // Estimated cost of a split tile's fix-up, in k-blocks of MMA time: on
 // GB300 the finishing unit's tail (bulk copy of the other partial, add,
 // store) measured ~3-4.5 µs against ~2 µs for a plain last epilogue, and the

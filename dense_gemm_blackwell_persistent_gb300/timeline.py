@@ -32,7 +32,8 @@ ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published",
 TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us",
           1: "producer_wait_response_us", 10: "mma_wait_response_us", 2: "epilogue_wait_response_us"}
 PROLOGUE = {1: "barriers_initialised", 2: "tensormaps_prefetched", 3: "cluster_arrived", 4: "cluster_passed",
-            5: "first_item_decoded", 6: "first_slot_free", 7: "first_loads_issued", 8: "mma_warp_has_tmem"}
+            5: "first_item_decoded", 6: "first_issuer_past_barrier", 7: "first_loads_issued",
+            8: "mma_warp_has_tmem"}
 
 
 def summarise(buf: np.ndarray, ctas: int) -> dict:

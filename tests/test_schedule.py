@@ -208,3 +208,16 @@ def test_dynamic_lists_cover_every_tile_once(dump_raw):
                 assert tile not in owner, (T, P, D, tile)
                 owner[tile] = c
         assert sorted(owner) == list(range(T)), (T, P, D)
+
+
+def test_fast_division_matches_the_operator(tmp_path):
+    """The multiply-and-shift divider the kernel decodes tiles with equals
+    integer division for every divisor up to 5000 and for divisors near
+    every power of two and at random up to 2^31 - 1, on numerators at the
+    edges of the range and at random."""
+    exe = str(tmp_path / "fastdiv_check")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, os.path.join(ROOT, "tests", "native", "fastdiv_check.cpp"),
+                    "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.startswith("ok "), out.stdout + out.stderr
+    assert int(out.stdout.split()[1]) > 1_000_000
