@@ -66,7 +66,7 @@ namespace gb300 {
 // %globaltimer stamps, wait totals and SM cycle counts in a device buffer of
 // kTraceSlots 64-bit words per CTA.  Without GEMM_TRACE the macros compile
 // to nothing.
-constexpr int kTraceSlots = 88;
+constexpr int kTraceSlots = 136;
 enum TraceSlot {
     kTrEntry = 0,         // %globaltimer at entry (thread 0; written at teardown)
     kTrClcWaitProducerNs = 1, kTrClcWaitEpiNs = 2,   // dynamic work list: time waiting for responses
@@ -87,7 +87,11 @@ enum TraceSlot {
     kTrClkPro = 64,       // + 0..8: SM cycles at the prologue steps (see timeline.PROLOGUE)
     kTrDynTile = 72,      // + 1 + r (r < 7): the list (cluster) that response r handed to this unit
     kTrSmid = 80,         // %smid of the CTA, + 1
+    kTrLastEpi = 88,      // + 12 * epilogue warp + step: SM cycles in the unit's last tile (see LastEpiStep)
 };
+// Steps of the last tile's epilogue, stamped by each epilogue warp's lane 0.
+enum LastEpiStep { kLeStart = 0, kLeFirstData = 1, kLeChunk = 2 /* + chunk c: its store issued */,
+                   kLeCommitted = 10, kLeStoresRead = 11 };
 #ifdef GEMM_TRACE
 #define GEMM_TR_ON() (p.trace && blockIdx.x < (unsigned)p.trace_ctas)
 #define GEMM_TR(slot) do { if (GEMM_TR_ON()) p.trace[blockIdx.x * kTraceSlots + (slot)] = global_timer_ns(); } while (0)
@@ -944,10 +948,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // store to finish reading, and each is stored as soon as it is
                 // staged.
                 if (row0 < p.M) {
+                    const int le = kTrLastEpi + 12 * (warp - 2);   // trace builds only
+                    (void)le;
+                    if (lane == 0) GEMM_TR_SET(le + kLeStart, (unsigned long long)clock64());
                     const uint32_t region = base + (uint32_t)(warp - 2) * (uint32_t)(kChunks * C::kSlotBytes);
                     uint32_t ra[32], rb[32];
                     tmem_ld_32x32b_x32(t_row, ra);
                     tmem_ld_wait(ra);
+                    if (lane == 0) GEMM_TR_SET(le + kLeFirstData, (unsigned long long)clock64());
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c) {
                         uint32_t(&cur)[32] = (c & 1) ? rb : ra;
@@ -958,9 +966,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         __syncwarp();
                         if (lane == 0 && col0 + c * kChunkCols < p.N)
                             tma_store_3d(&tmC, region + (uint32_t)(c * C::kSlotBytes), col0 + c * kChunkCols, row0, bt);
+                        if (lane == 0 && c < 8) GEMM_TR_SET(le + kLeChunk + c, (unsigned long long)clock64());
                         if (c + 1 < kChunks) tmem_ld_wait(nxt);
                     }
                     if (lane == 0) bulk_commit_group();
+                    if (lane == 0) GEMM_TR_SET(le + kLeCommitted, (unsigned long long)clock64());
                 }
             } else if (w.ncontrib == 1) {
                 if (row0 < p.M) {
@@ -1069,6 +1079,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // Only the staging buffers' reads must be done before shared memory
         // goes away; the writes to C complete with the grid.
         if (lane == 0) bulk_wait_group_read<0>();
+        if (lane == 0) GEMM_TR_SET(kTrLastEpi + 12 * (warp - 2) + kLeStoresRead, (unsigned long long)clock64());
         __syncwarp();
         if (warp == 2 && lane == 0) GEMM_TR(kTrEpiDone);
         if (warp == 2 && lane == 0) GEMM_TR_SET(kTrClcWaitEpiNs, clc_wait_ns);

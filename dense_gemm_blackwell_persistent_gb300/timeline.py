@@ -81,6 +81,20 @@ def summarise(buf: np.ndarray, ctas: int) -> dict:
             if ok.any():
                 d = (v[ok] - c0[have][ok]).astype(np.int64)
                 out[f"cycles_to_{name}"] = [int(d.min()), int(np.median(d)), int(d.max()), int(ok.sum())]
+    # SM cycles of the unit's last tile's epilogue, per epilogue warp, from
+    # the warp's first step (accumulator ready): median over CTAs
+    for wq in range(4):
+        b = 88 + 12 * wq
+        st = t[:, b]
+        have = st > 0
+        if not have.any():
+            continue
+        steps = []
+        for k in range(1, 12):
+            v = t[have, b + k]
+            ok = v > 0
+            steps.append(int(np.median(v[ok] - st[have][ok])) if ok.any() else None)
+        out[f"last_epilogue_cycles_warp{wq + 2}"] = steps
     for col, name in TOTALS.items():
         v = t[:, col][t[:, col] > 0] / 1e3
         if v.size:
