@@ -36,6 +36,7 @@ GEMM_OPT_DYNAMIC = 9
 GEMM_OPT_FAIL_ENCODE = 10
 GEMM_OPT_VISIBLE_DEVICES = 11
 GEMM_OPT_CLOCK_LOG = 12
+GEMM_OPT_PDL = 13
 GEMM_K_MAJOR, GEMM_A_MN_MAJOR, GEMM_B_MN_MAJOR = 0, 1, 2
 
 # GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps),

@@ -141,6 +141,7 @@ struct gemm_plan {
     int stall_test = 0;           // tests of the timeout path only
     int fail_encode = 0;          // tests of the error path only: the encoder rejects every map
     int visible_devices = 1;      // GPUs the process sees (multicast only with one)
+    int pdl = 1;                  // launch as a programmatic dependent of the stream's previous kernel
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
@@ -371,13 +372,19 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)ki.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the grid may be scheduled before the
+    // stream's previous kernel has finished, so that its launch and set-up
+    // overlap that kernel's end; the kernel waits (griddepcontrol.wait) for
+    // the previous grids before touching global memory.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = plan->pdl ? 2 : 1;
     if (plan->d_clock != nullptr) {
         const int64_t slot = plan->clock_next.fetch_add(1) % plan->clock_cap;
         p.clock_rec = plan->d_clock + 2 * slot;
@@ -555,6 +562,10 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
             plan->visible_devices = n;
             return GEMM_OK;
         }
+        case GEMM_OPT_PDL:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            plan->pdl = (int)value;
+            return GEMM_OK;
         case GEMM_OPT_CLOCK_LOG: {
             if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
             int prev = 0;

@@ -652,6 +652,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     if constexpr (kCluster > 1) cluster_wait();
     if (threadIdx.x == 0) GEMM_TR_CLK(4);
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream, this grid may have started while that kernel still runs: the
+    // set-up above touches only this CTA's shared memory, TMEM and the kernel
+    // parameters.  Every thread waits here for the previous grids' completion
+    // before any load of A or B, any store of C and any use of the plan's
+    // device memory.
+    griddep_wait();
     if (warp == 2 && pre_ok) {
 #ifdef GEMM_DEBUG
         pre_ok = GEMM_WARP_CHECK(item_ok(w_first) && rows_ok(pre_rows[0], pre_rows[1], pre_rows[2]), kChkOperandRows);
@@ -756,6 +763,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
+            griddep_launch_dependents();   // no more loads from this warp
             GEMM_TR_SET(kTrEmptyWaitNs, empty_wait_ns);
             if (lane == 0) GEMM_TR_SET(kTrClcWaitProducerNs, clc_wait_ns);
             (void)empty_wait_ns;
@@ -870,6 +878,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
         }
         __syncwarp();
+        griddep_launch_dependents();   // no more MMAs in this CTA
     } else {
         // ================= epilogue warps
         const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad+31
@@ -942,6 +951,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 break;
             const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + b * kAccStride;
             if (w.ncontrib == 1 && gn == 0) {
+                // The last tile's loads and MMAs are done: a programmatic
+                // dependent grid may be scheduled (its CTAs start as this
+                // grid's exit, and wait for its completion before reading).
+                griddep_launch_dependents();
                 // The unit's last tile: nothing overlaps its epilogue, and its
                 // operand ring is idle (no later loads, every MMA done), so each
                 // chunk gets its own box there: no chunk waits for an earlier
@@ -1076,6 +1089,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             w = nw;
             g = gn;
         }
+        griddep_launch_dependents();   // (again, if the loop ended without a last whole tile)
         // Only the staging buffers' reads must be done before shared memory
         // goes away; the writes to C complete with the grid.
         if (lane == 0) bulk_wait_group_read<0>();

@@ -63,6 +63,16 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this
+// one depends on have completed and their memory operations are visible (no
+// effect when it was not launched as a dependent).  griddep_launch_dependents:
+// this CTA allows a grid launched after it as a programmatic dependent to be
+// scheduled (once every CTA of this grid has done so or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // CTA-local named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

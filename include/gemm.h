@@ -167,6 +167,16 @@ typedef enum {
                                     default), read by gemm_plan_clock_log.  Setting it
                                     allocates (or frees) value × 16 bytes of device
                                     memory and waits for the device                  */
+    GEMM_OPT_PDL = 13,           /* 1 (default): launch as a programmatic dependent of
+                                    the kernel before it on the stream, so that this
+                                    launch and its set-up (barriers, TMEM, first work
+                                    item) overlap that kernel's end; every thread then
+                                    waits for the earlier grids to complete before any
+                                    access to A, B, C or the plan's device memory.  The
+                                    kernel also signals its own dependents once its
+                                    last tiles' loads and MMAs are issued.  A kernel
+                                    launched after it without that attribute is
+                                    ordered as usual.  0: plain stream order        */
     GEMM_OPT_VISIBLE_DEVICES = 11 /* GPUs the plan counts as visible to the process,
                                     1..1024 (0 = default: cudaGetDeviceCount at plan
                                     creation).  TMA multicast stays within one GPU's

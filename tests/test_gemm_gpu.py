@@ -1094,6 +1094,78 @@ def test_operands_must_be_device_memory_of_the_run_device(g, fresh_plan):
     assert np.array_equal(got, C_ref)
 
 
+def signed_permutation(n, seed):
+    """An n×n matrix with one ±1 per row and column (a signed permutation)."""
+    gen = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n, generator=gen)
+    sign = torch.randint(0, 2, (n,), generator=gen) * 2 - 1
+    P = torch.zeros((n, n), dtype=torch.float32)
+    P[torch.arange(n), perm] = sign.float()
+    return P
+
+
+# (M, K, options): one wave of 224-wide pair tiles; many waves with the
+# partial last wave handed out at run time; the stream-K tail on a CTA cap;
+# the 4-CTA multicast unit (K rows not a multiple of 128 bytes)
+PDL_CHAINS = [(1024, 4096, {}), (4096, 2048, {9: 1}), (1300, 1096, {5: 1, 3: 14, 6: 0}), (1000, 1256, {6: 1})]
+
+
+@pytest.mark.parametrize("pdl", [1, 0], ids=["pdl", "stream_order"])
+@pytest.mark.parametrize("chain", PDL_CHAINS, ids=lambda c: f"{c[0]}x{c[1]}")
+def test_back_to_back_chain_reads_each_result(g, fresh_plan, pdl, chain):
+    """Sixteen products launched back to back on one stream, each reading the
+    previous one's output as its A: X_{i+1} = X_i · P_iᵀ with P_i a signed
+    permutation, so every X_i is a signed column permutation of X_0 (values
+    in {-1, 0, 1}, exact in f16 at any length).  With programmatic dependent
+    launch each grid may start while the previous one runs; it must still
+    read the finished X_i.  Every intermediate is checked against the same
+    permutations applied on the CPU."""
+    M, K, opts = chain
+    if opts.get(6) == 1 and torch.cuda.device_count() > 1:
+        pytest.skip("the library multicasts only while one GPU is visible")
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_PDL, pdl)
+    for k, v in opts.items():
+        g.gemm_plan_set_option(fresh_plan, k, v)
+    gen = torch.Generator().manual_seed(M + K)
+    X0 = (torch.randint(0, 3, (M, K), generator=gen) - 1).to(torch.float16)
+    Ps = [signed_permutation(K, 100 * M + i) for i in range(16)]
+    xs = [X0.cuda()] + [torch.full((M, K), float("nan"), dtype=torch.float16, device="cuda") for _ in range(16)]
+    Pd = [P.to(torch.float16).cuda() for P in Ps]
+    st = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    for i in range(16):
+        g.gemm_plan_run(fresh_plan, xs[i].data_ptr(), Pd[i].data_ptr(), xs[i + 1].data_ptr(), M, K, K, wl.F16,
+                        wl.F16, st)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(fresh_plan) == 0
+    want = X0.float()
+    for i in range(16):
+        want = want @ Ps[i].t()
+        got = xs[i + 1].float().cpu()
+        assert torch.equal(got, want), f"product {i}: {int((got != want).sum())} entries differ"
+
+
+def test_launch_right_after_torch_kernels_reads_their_output(g, fresh_plan):
+    """Torch kernels rewrite A just before each launch (no programmatic
+    signal from them): the product must see the rewritten A every time."""
+    M, N, K = 1024, 1040, 1024
+    A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.ones((N, K), dtype=torch.bfloat16, device="cuda")
+    Cs = [torch.full((M, N), float("nan"), device="cuda") for _ in range(8)]
+    st = torch.cuda.current_stream().cuda_stream
+    for i in range(8):
+        A.fill_(float(i - 3))                 # every entry i - 3: each C entry is K * (i - 3)
+        g.gemm_plan_run(fresh_plan, A.data_ptr(), B.data_ptr(), Cs[i].data_ptr(), M, N, K, wl.BF16, wl.F32, st)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(fresh_plan) == 0
+    for i in range(8):
+        assert bool((Cs[i] == K * (i - 3)).all()), i
+    import ctypes
+    for bad in (-1, 2):
+        assert g.raw_status("gemm_plan_set_option", ctypes.c_void_p(fresh_plan), g.GEMM_OPT_PDL,
+                            ctypes.c_int64(bad)) == g.GEMM_ERR_INVALID_ARG
+
+
 def test_clock_log_records_each_launch(g, fresh_plan):
     """GEMM_OPT_CLOCK_LOG keeps, per launch, the SM cycles and nanoseconds of
     the first CTA's lifetime: one record per launch, oldest first, a
