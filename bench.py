@@ -63,7 +63,7 @@ def parse_args():
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core issue-rate probe")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the context lines (L2-resident run, other workloads, sustained runs)")
+                    help="skip the context lines (back-to-back run, other workloads, sustained runs)")
     ap.add_argument("--sustained-s", type=float, default=4.0, help="seconds of each sustained run (0 = none)")
     return ap.parse_args()
 
@@ -546,6 +546,50 @@ def sustained_line(torch, g, args, name, seconds, stream, local):
     return line
 
 
+def back_to_back_line(torch, g, args, w, A, B, C, out_t, stream, local, n=200):
+    """The same workload with L2 left warm: n launches enqueued back to back
+    between two events (no host gap inside; the library's launches overlap
+    their set-up with the previous launch's end), time ÷ n; cuBLAS the same
+    way on the same inputs."""
+    plan = make_plan(g, args, local)
+    sp = stream.cuda_stream
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        for _ in range(10):
+            g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype, sp)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            g.gemm_plan_run(plan, A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.dtype, w.out_dtype, sp)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if g.gemm_plan_status(plan) != 0:
+            raise SystemExit(f"{w.name}: device status error in the back-to-back run")
+    finally:
+        g.gemm_plan_destroy(plan)
+    ms = e0.elapsed_time(e1) / n
+    line = {"value": w.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_launch": ms, "launches": n,
+            "how": "launches back to back between two events, operands resident in L2 (no flush), "
+                   "programmatic dependent launch on"}
+    if not args.no_cublas:
+        call, how = cublas_call(torch, w, A, B, out_t)
+        try:
+            for _ in range(10):
+                call()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_ref = e0.elapsed_time(e1) / n
+            line["cublas_reference"] = {"value": w.flops / (ms_ref / 1e3) / 1e12, "unit": "TFLOP/s",
+                                        "ms_per_launch": ms_ref, "how": f"{how}, the same way"}
+        except (RuntimeError, NotImplementedError, TypeError) as e:
+            line["cublas_reference"] = {"unavailable": f"{how}: " + str(e).splitlines()[0][:200]}
+    return line
+
+
 def main():
     args = parse_args()
     w = wl.WORKLOADS[args.workload]
@@ -628,17 +672,10 @@ def main():
     g.gemm_plan_destroy(plan)
 
     # Context lines, outside the timed region (rank 0 only): the same
-    # workload with L2 left warm between launches, the other workloads of the
+    # workload back to back with L2 left warm, the other workloads of the
     # benchmark set, and seconds-long back-to-back runs at the power limit.
     if rank == 0 and not args.no_extra:
-        resident = g.gemm_plan_create(local)
-        try:
-            ms_res, rec_res, _ = time_launches(torch, g, resident, w, A, B, C, stream, 200, 5, None)
-        finally:
-            g.gemm_plan_destroy(resident)
-        extra["l2_resident"] = {"value": w.flops / (statistics.mean(ms_res) / 1e3) / 1e12, "unit": "TFLOP/s",
-                                "ms_mean": statistics.mean(ms_res), "kernel_clock": kernel_clock(rec_res),
-                                "how": "200 launches, no flush between them (operands stay in L2), default plan"}
+        extra["back_to_back"] = back_to_back_line(torch, g, args, w, A, B, C, out_t, stream, local)
         del A, B, C
         others = {}
         for name in OTHER_WORKLOADS:
