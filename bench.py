@@ -705,7 +705,7 @@ def main():
                        "inputs": w.describe(), "parallelism": f"replicas x{world}",
                        "l2": "not flushed" if args.no_flush else "flushed before every step (512 MiB write)",
                        "launch": timed_launch,
-                       "tile_per_mma": f"{128 * (args.cta_pair or 2)}x{timed_launch['tile_n']}x"
+                       "tile_per_mma": f"{128 * min(timed_launch['ctas_per_unit'], 2)}x{timed_launch['tile_n']}x"
                                        f"{128 // wl.ELEM_BYTES[w.dtype]}",
                        "vs_baseline_ref": "pages' 293.6 TFLOP/s, Mojo part-2 kernel 4 on B200 (context)"},
             "roofline": roof,

@@ -130,7 +130,7 @@ struct gemm_plan {
     int device = 0;
     int sm_count = 0;
     int max_ctas[5] = {0, 0, 0, 0, 0};  // resident CTAs per unit size 1, 2, 4 (index by size)
-    int pair = 2;                 // CTAs per MMA
+    int pair = 0;                 // CTAs per MMA: 1, 2, or 0 = chosen per problem (launch_auto_pair)
     int multicast = -1;           // with pairs: share B across two pairs (1), never (0), auto (-1)
     int group_m = 0;
     int cap_ctas = 0;
@@ -242,8 +242,16 @@ static_assert(kLaunchRowsPerCta == kRowsPerCta && kLaunchMnBox == kMnBoxElems, "
 static_assert(kErrTimeout == GEMM_ERR_TIMEOUT && kErrCuda == GEMM_ERR_CUDA && kErrInternal == GEMM_ERR_INTERNAL,
               "device-side status codes are the header's");
 
-int unit_ctas(const gemm_plan* plan, int64_t K, int in_dtype, int layout) {
-    return launch_unit_ctas(plan->pair, plan->multicast, plan->visible_devices, K, elem_bytes(in_dtype), layout);
+// CTAs per MMA for this problem: the plan's choice, or automatic (a forced
+// multicast unit is made of pairs).
+int cta_pair(const gemm_plan* plan, int64_t M, int64_t N, int64_t batch) {
+    if (plan->pair > 0) return plan->pair;
+    if (plan->multicast == 1) return 2;
+    return launch_auto_pair(M, N, batch, plan->max_ctas[2] / 2, plan->max_ctas[1]);
+}
+
+int unit_ctas(const gemm_plan* plan, int pair, int64_t K, int in_dtype, int layout) {
+    return launch_unit_ctas(pair, plan->multicast, plan->visible_devices, K, elem_bytes(in_dtype), layout);
 }
 
 // Resident units a launch may use.
@@ -273,9 +281,9 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
                                                                   stride16);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    const int pair = plan->pair;
+    const int pair = cta_pair(plan, M, N, batch.count);
     if (pair == 2 && plan->multicast == 1 && plan->visible_devices != 1) return GEMM_ERR_UNSUPPORTED;
-    const int cluster = unit_ctas(plan, K, dtype, layout);
+    const int cluster = unit_ctas(plan, pair, K, dtype, layout);
     const int bn = choose_tile_n(plan, M, N, cluster, layout, batch.count);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
     const bool pad = (layout & GEMM_B_MN_MAJOR) && !launch_b_boxes_exact(bn, cluster);
@@ -517,7 +525,7 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
     switch (option) {
         case GEMM_OPT_CTA_PAIR:
-            if (value != 1 && value != 2) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             plan->pair = (int)value;
             return GEMM_OK;
         case GEMM_OPT_GROUP_M:

@@ -23,6 +23,21 @@ constexpr int kLaunchWidths[kLaunchTileWidths] = {256, 224, 192, 160, 128};   //
 constexpr int kLaunchRowsPerCta = 128;   // rows of A per CTA (TMEM lanes)
 constexpr int kLaunchMnBox = 64;         // elements of M or N per MN-major TMA box
 
+// CTAs per MMA when the caller leaves it to the library (option 0): single
+// CTAs for problems too small to fill half a wave of CTA pairs, as long as
+// their 128×128 tiles still fit in one wave of single CTAs; pairs
+// otherwise.  A pair's launch and cluster set-up cost more than it saves
+// there: measured on GB300 (flushed, single vs pair, µs): 256³ 8.2 vs 10.3,
+// 768³ 10.6 vs 12.3, 1024³ 12.3 vs 12.7, 256×4096×1024 12.1 vs 14.0,
+// 128×4096×4096 23.5 vs 24.7, 2048×256×4096 22.2 vs 23.9; from a full wave
+// of pair tiles on the pairs win clearly (1024×4096×4096: 76 pair tiles).
+// `pair_units` and `single_units`: resident units of each size.
+inline int launch_auto_pair(int64_t M, int64_t N, int64_t batch, int64_t pair_units, int64_t single_units) {
+    const int64_t pair_tiles = batch * ((M + 2 * kLaunchRowsPerCta - 1) / (2 * kLaunchRowsPerCta)) * ((N + 255) / 256);
+    const int64_t single_tiles = batch * ((M + kLaunchRowsPerCta - 1) / kLaunchRowsPerCta) * ((N + 127) / 128);
+    return (2 * pair_tiles <= pair_units && single_tiles <= single_units) ? 1 : 2;
+}
+
 // CTAs per work unit: 1 (pair = 1), 2 (a CTA pair) or 4 (two pairs sharing B
 // through TMA multicast).  Multicast is used only while the process sees
 // a single GPU, so no code of a process that may drive several GPUs

@@ -105,8 +105,11 @@ typedef enum { GEMM_K_MAJOR = 0, GEMM_A_MN_MAJOR = 1, GEMM_B_MN_MAJOR = 2 } gemm
 /* Plan options (gemm_plan_set_option).  For tuning sweeps and tests; the
  * defaults are what the library picks itself. */
 typedef enum {
-    GEMM_OPT_CTA_PAIR = 1,       /* 2 (default): 2-CTA pairs, 256×BN tile per pair;
-                                    1: one CTA per 128×BN tile                          */
+    GEMM_OPT_CTA_PAIR = 1,       /* 2: 2-CTA pairs, 256×BN tile per pair; 1: one CTA
+                                    per 128×BN tile; 0 (default): pairs, except for
+                                    problems under half a wave of pair tiles that fit
+                                    one wave of 128×128 single-CTA tiles (there a
+                                    pair's set-up costs more than it saves)         */
     GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
     GEMM_OPT_TILE_N = 4,         /* tile width: 256, 224, 192, 160 or 128 (0 = default:

@@ -500,6 +500,7 @@ def test_multicast_only_with_one_visible_gpu(g, fresh_plan):
     C_ref, _ = oracle_full(A, B)
     Ad, Bd = A.cuda(), B.cuda()
     opt = g.GEMM_OPT_VISIBLE_DEVICES
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_CTA_PAIR, 2)   # pairs: this product is small enough for single CTAs
     try:
         for visible, unit in ((1, 4), (2, 2)):
             g.gemm_plan_set_option(fresh_plan, opt, visible)

@@ -27,7 +27,7 @@ def choose(tmp_path_factory):
     exe = str(tmp_path_factory.mktemp("launch") / "launch_dump")
     subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, "-I", INCLUDE, SRC, "-o", exe], check=True)
 
-    def run(M, N, K, ib=2, layout=0, pair=2, mc=-1, visible=1, forced=0, batch=1, mode=-1, capped=0, sk=0,
+    def run(M, N, K, ib=2, layout=0, pair=0, mc=-1, visible=1, forced=0, batch=1, mode=-1, capped=0, sk=0,
             resident=GB300):
         line = f"{M} {N} {K} {ib} {layout} {pair} {mc} {visible} {forced} {batch} {mode} {capped} {sk} " \
                f"{resident[0]} {resident[1]} {resident[2]}\n"
@@ -73,7 +73,7 @@ def test_tile_width_fills_whole_waves(choose):
     cycles = {256: 520, 224: 453, 192: 432, 160: 429, 128: 485}
     for M, N, K in [(2048, 2048, 2048), (3072, 3072, 3072), (6144, 6144, 6144), (4096, 8192, 1024),
                     (1000, 776, 1256), (256, 256, 256), (4096, 4096, 4096), (8192, 8192, 8192)]:
-        r = choose(M, N, K)
+        r = choose(M, N, K, pair=2)
         units = {2: 76, 4: 36}[r["unit"]]           # pairs, or the 4-CTA unit for unaligned rows
         tiles_m = -(-M // (128 * r["unit"]))
         best, best_cost = 0, None
@@ -113,3 +113,24 @@ def test_dynamic_list_rules(choose):
     assert r["dynamic"] and (r["units"], r["waves"]) == (r["tiles"], 1)
     # mode 0: static
     assert not choose(8192, 8192, 8192, mode=0)["dynamic"]
+
+
+def test_single_ctas_for_small_problems(choose):
+    """Left to the library (pair option 0), problems under half a wave of
+    256×256 pair tiles whose 128×128 single-CTA tiles fit one wave run on
+    single CTAs (a pair's set-up costs more than it saves there); from half
+    a wave of pair tiles on, pairs (and the multicast unit where it applies)."""
+    assert choose(256, 256, 256)["unit"] == 1                 # 1 pair tile
+    assert choose(1024, 1024, 1024)["unit"] == 1              # 16 pair tiles, 64 single tiles
+    assert choose(128, 4096, 4096)["unit"] == 1               # 16 pair tiles, 32 single tiles
+    assert choose(1000, 776, 1256)["unit"] == 1               # misaligned rows, but small: single CTAs
+    assert choose(1024, 4096, 4096)["unit"] == 2              # 64 pair tiles: more than half a wave
+    assert choose(1536, 1536, 1024)["unit"] == 1              # 36 pair tiles, 144 single tiles: one wave
+    assert choose(1536, 1792, 1024)["unit"] == 2              # 42 pair tiles
+    assert choose(1664, 1664, 1024)["unit"] == 2              # 49 pair tiles
+    assert choose(1024, 1024, 128, batch=32)["unit"] == 2     # batched: 512 pair tiles
+    assert choose(2048, 2048, 2048)["unit"] == 2              # 64 pair tiles
+    # an explicit choice or a forced multicast unit is honoured
+    assert choose(256, 256, 256, pair=2)["unit"] == 2
+    assert choose(1000, 776, 1256, mc=1)["unit"] == 4
+    assert choose(4096, 4096, 4096, pair=1)["unit"] == 1
