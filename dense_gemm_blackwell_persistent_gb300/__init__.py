@@ -37,6 +37,7 @@ GEMM_OPT_FAIL_ENCODE = 10
 GEMM_OPT_VISIBLE_DEVICES = 11
 GEMM_OPT_CLOCK_LOG = 12
 GEMM_OPT_PDL = 13
+GEMM_OPT_SPLIT_K = 14
 GEMM_K_MAJOR, GEMM_A_MN_MAJOR, GEMM_B_MN_MAJOR = 0, 1, 2
 
 # GB300_GEMM_VARIANT=trace selects the GEMM_TRACE build (timeline stamps),
@@ -71,6 +72,7 @@ _lib.gemm_run_noalloc.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _
 _lib.gemm_plan_status.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_grid.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_tile_n.argtypes = [_vp, ctypes.POINTER(_int)]
+_lib.gemm_plan_last_split.argtypes = [_vp, ctypes.POINTER(_int)]
 _lib.gemm_plan_last_launch.argtypes = [_vp] + [ctypes.POINTER(_int)] * 5
 _lib.gemm_plan_destroy.argtypes = [_vp]
 _lib.gemm_plan_trace.argtypes = [_vp, _vp, ctypes.c_size_t, ctypes.POINTER(_int), ctypes.POINTER(_int)]
@@ -81,7 +83,7 @@ _lib.gemm_strerror.argtypes = [_int]
 _lib.gemm_strerror.restype = ctypes.c_char_p
 for _name in ("gemm_plan_create", "gemm_plan_set_option", "gemm_run", "gemm_run_noalloc", "gemm_plan_run",
               "gemm_plan_run_host", "gemm_plan_run_layout", "gemm_plan_run_batched", "gemm_plan_status", "gemm_plan_last_grid", "gemm_plan_last_tile_n",
-              "gemm_plan_last_launch",
+              "gemm_plan_last_launch", "gemm_plan_last_split",
               "gemm_plan_trace", "gemm_plan_clock_log", "gemm_plan_destroy", "gemm_probe_mma_rate",
               "gemm_probe_mma_rate_n"):
     getattr(_lib, _name).restype = _int
@@ -173,6 +175,12 @@ def gemm_plan_last_grid(plan: int) -> int:
     n = _int(0)
     _check(_lib.gemm_plan_last_grid(_vp(plan), ctypes.byref(n)), "gemm_plan_last_grid")
     return n.value
+
+
+def gemm_plan_last_split(plan: int) -> int:
+    v = _int()
+    _check(_lib.gemm_plan_last_split(_vp(plan), ctypes.byref(v)), "gemm_plan_last_split")
+    return v.value
 
 
 def gemm_plan_last_tile_n(plan: int) -> int:

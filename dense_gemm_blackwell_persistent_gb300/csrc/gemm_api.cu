@@ -78,14 +78,15 @@ int get_encoder(EncodeTiledFn* out) {
 // path) replaces the driver's encoder by one that rejects the map.
 int encode_3d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t cols, uint64_t count,
               uint64_t stride, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle,
-              CUtensorMapL2promotion promo, bool fake_reject = false) {
+              CUtensorMapL2promotion promo, bool fake_reject = false, uint64_t pitch = 0) {
     EncodeTiledFn enc;
     int rc = get_encoder(&enc);
     if (rc != GEMM_OK) return rc;
     const uint64_t eb = (uint64_t)elem_bytes(dt);
-    if (count <= 1) stride = rows * cols;
+    if (pitch == 0) pitch = cols;   // elements from one row to the next
+    if (count <= 1) stride = rows * pitch;
     cuuint64_t dims[3] = {cols, rows, count < 1 ? 1 : count};
-    cuuint64_t strides[2] = {cols * eb, stride * eb};
+    cuuint64_t strides[2] = {pitch * eb, stride * eb};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fake_reject ? CUDA_ERROR_INVALID_VALUE
@@ -95,10 +96,14 @@ int encode_3d(CUtensorMap* map, int dt, const void* ptr, uint64_t rows, uint64_t
 }
 
 // A batch of products: `count` problems with A, B, C `sa`, `sb`, `sc`
-// elements apart (0 for A or B: every problem uses the same matrix).
+// elements apart (0 for A or B: every problem uses the same matrix).  `lda`,
+// `ldb`: elements from one row of a K-major A or B to the next, when larger
+// than K (the K slices of a split product are column slices of A and B);
+// 0 = K.
 struct Batch {
     int64_t count = 1;
     int64_t sa = 0, sb = 0, sc = 0;
+    int64_t lda = 0, ldb = 0;
 };
 
 // tcgen05 instruction descriptor: f32 accumulator, A and B K-major, M×N.
@@ -124,6 +129,40 @@ __global__ void fill_zero_kernel(uint4* __restrict__ c, size_t n16, int64_t coun
     }
 }
 
+// The reduction of a split product: C = Σ_s W_s, s = 0..S-1 in order (W_s
+// the fp32 partial of K slice s, `slice` floats apart), converted to C's
+// type (round to nearest even), four elements per thread.  Launched as a
+// programmatic dependent of the slices' GEMM: it waits for that grid before
+// reading the partials.
+template <int kOut>
+__global__ void splitk_reduce_kernel(const float4* __restrict__ w, void* __restrict__ c, size_t n4, size_t slice4,
+                                     int slices) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const size_t step = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += step) {
+        float4 acc = __ldcg(w + i);
+        for (int s = 1; s < slices; ++s) {
+            const float4 v = __ldcg(w + (size_t)s * slice4 + i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if constexpr (kOut == GEMM_F32) {
+            reinterpret_cast<float4*>(c)[i] = acc;
+        } else if constexpr (kOut == GEMM_BF16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            reinterpret_cast<uint2*>(c)[i] =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        } else {
+            __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+            reinterpret_cast<uint2*>(c)[i] =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace
 
 struct gemm_plan {
@@ -142,6 +181,12 @@ struct gemm_plan {
     int fail_encode = 0;          // tests of the error path only: the encoder rejects every map
     int visible_devices = 1;      // GPUs the process sees (multicast only with one)
     int pdl = 1;                  // launch as a programmatic dependent of the stream's previous kernel
+    int split_k = -1;             // K slices: -1 automatic (launch_split_k), 0 never, 2..32 asked for
+    // Split products share the stream-K workspace: their runs are ordered
+    // one after the other on the GPU, whatever stream they come from, by
+    // this event (the last split product's reduction), under split_mu.
+    std::mutex split_mu;
+    cudaEvent_t split_ev = nullptr;
     float* d_partials = nullptr;  // stream-K workspace: one partial-tile slot per unit
     int* d_flags = nullptr;       // stream-K "partial published" flags
     unsigned long long* d_trace = nullptr;  // GEMM_TRACE builds: kTraceSlots words per CTA
@@ -160,6 +205,7 @@ struct gemm_plan {
     int last_unit = 0;
     int last_dp_waves = 0;
     int last_sk_tiles = 0;
+    int last_split = 1;
     std::mutex host_mu;           // serialises gemm_plan_run_host's buffers
     void* hbuf[3] = {nullptr, nullptr, nullptr};
     size_t hcap[3] = {0, 0, 0};
@@ -270,8 +316,12 @@ bool dynamic_lists(const gemm_plan* plan, int64_t tiles, int64_t resident, int* 
                                 waves);
 }
 
+int launch_split(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                 int dtype, int out_dtype, cudaStream_t stream, int slices, int pair);
+size_t partials_bytes(const gemm_plan* plan);
+
 int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int dtype,
-           int out_dtype, cudaStream_t stream, int layout = 0, const Batch& batch = Batch()) {
+           int out_dtype, cudaStream_t stream, int layout = 0, const Batch& batch = Batch(), int pair_forced = 0) {
     if (K == 0) {
         // N·out_bytes and, for batches, the C stride in bytes are 16-byte multiples (checked by the callers)
         const size_t n16 = (size_t)M * (size_t)N * elem_bytes(out_dtype) / 16;
@@ -281,11 +331,24 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
                                                                   stride16);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    const int pair = cta_pair(plan, M, N, batch.count);
+    const int pair = pair_forced > 0 ? pair_forced : cta_pair(plan, M, N, batch.count);
     if (pair == 2 && plan->multicast == 1 && plan->visible_devices != 1) return GEMM_ERR_UNSUPPORTED;
     const int cluster = unit_ctas(plan, pair, K, dtype, layout);
     const int bn = choose_tile_n(plan, M, N, cluster, layout, batch.count);
     if (bn == 0) return GEMM_ERR_UNSUPPORTED;
+    // Few tiles and a long K: split K over more units (one plain product,
+    // K-major operands, the workspace free of stream-K).
+    if (batch.count == 1 && layout == 0 && plan->split_k != 0 && !plan->stream_k && plan->d_partials != nullptr &&
+        plan->cap_ctas == 0) {
+        const int64_t tile_m = (int64_t)kRowsPerCta * cluster;
+        const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + bn - 1) / bn);
+        const int64_t kbe = kblock_elems(dtype);
+        const int64_t kb = (K + kbe - 1) / kbe;
+        const int slices = K % kbe == 0 ? launch_split_k(plan->split_k, tiles, resident_units(plan, cluster), kb,
+                                                         M * N, (int64_t)(partials_bytes(plan) / sizeof(float)))
+                                        : 1;
+        if (slices > 1) return launch_split(plan, A, B, C, M, N, K, dtype, out_dtype, stream, slices, pair);
+    }
     const bool pad = (layout & GEMM_B_MN_MAJOR) && !launch_b_boxes_exact(bn, cluster);
     const KernelInfo ki = kernel_info(cluster, bn, out_dtype, is_fp8(dtype) ? 1 : 0, pad);
     if (ki.fn == nullptr) return GEMM_ERR_INVALID_ARG;
@@ -349,7 +412,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     // measured 4000×4000×5000 106.8 → 98.6 µs and 8000×8000×5000 399 → 376
     // (4000×3000×5000 level), while on aligned rows 256 bytes is faster
     // (1024×4096×4096: 28.7 vs 29.7 µs).  B keeps 256 bytes either way.
-    const int64_t a_pitch = ((layout & GEMM_A_MN_MAJOR) ? M : K) * elem_bytes(dtype);
+    const int64_t a_pitch = ((layout & GEMM_A_MN_MAJOR) ? M : (batch.lda > 0 ? batch.lda : K)) * elem_bytes(dtype);
     const CUtensorMapL2promotion promo_a =
         a_pitch % 128 != 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     const uint64_t na = p.a_batched ? (uint64_t)batch.count : 1, nb = p.b_batched ? (uint64_t)batch.count : 1;
@@ -357,14 +420,14 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
                  ? encode_3d(&tmA, dtype, A, (uint64_t)K, (uint64_t)M, na, (uint64_t)batch.sa, (uint32_t)kbe,
                              kMnBoxElems, CU_TENSOR_MAP_SWIZZLE_128B, promo_a)
                  : encode_3d(&tmA, dtype, A, (uint64_t)M, (uint64_t)K, na, (uint64_t)batch.sa, kRowsPerCta,
-                             (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B, promo_a);
+                             (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B, promo_a, false, (uint64_t)batch.lda);
     if (rc == GEMM_OK)
         rc = (layout & GEMM_B_MN_MAJOR)
                  ? encode_3d(&tmB, dtype, B, (uint64_t)K, (uint64_t)N, nb, (uint64_t)batch.sb, (uint32_t)kbe,
                              kMnBoxElems, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
                  : encode_3d(&tmB, dtype, B, (uint64_t)N, (uint64_t)K, nb, (uint64_t)batch.sb,
                              (uint32_t)(bn / cluster), (uint32_t)kbe, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, false, (uint64_t)batch.ldb);
     // C: 32-row × 32-column store boxes; 128-byte rows (fp32) or 64-byte rows (16-bit)
     if (rc == GEMM_OK)
         rc = encode_3d(&tmC, out_dtype, C, (uint64_t)M, (uint64_t)N, (uint64_t)batch.count, (uint64_t)batch.sc, 32,
@@ -408,6 +471,68 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     plan->last_unit = cluster;
     plan->last_dp_waves = dyn ? (dyn_units == p.num_tiles ? 0 : dyn_waves) : p.sched.dp_waves;
     plan->last_sk_tiles = p.sched.sk_tiles;
+    plan->last_split = 1;
+    return GEMM_OK;
+}
+
+// A split product: the K slices are a batch of `slices` products over column
+// slices of A and B (K / slices columns each, rows still K apart), each
+// writing its fp32 partial into the plan's workspace, on units of `pair` CTAs
+// per MMA as the unsplit product would use; then the reduction sums the
+// partials in slice order into C.  Split products of one plan share the
+// workspace, so each waits on the GPU for the previous one's reduction
+// (plan->split_ev) unless the stream is being captured into a graph.
+int launch_split(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                 int dtype, int out_dtype, cudaStream_t stream, int slices, int pair) {
+    std::lock_guard<std::mutex> lk(plan->split_mu);
+    if (plan->split_ev == nullptr &&
+        cudaEventCreateWithFlags(&plan->split_ev, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        plan->split_ev = nullptr;
+        return GEMM_ERR_CUDA;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    const bool ordered = cap == cudaStreamCaptureStatusNone;
+    if (ordered && cudaStreamWaitEvent(stream, plan->split_ev, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    Batch bt;
+    bt.count = slices;
+    bt.sa = bt.sb = K / slices;
+    bt.sc = M * N;
+    bt.lda = bt.ldb = K;
+    int rc = launch(plan, A, B, plan->d_partials, M, N, K / slices, dtype, GEMM_F32, stream, 0, bt, pair);
+    if (rc != GEMM_OK) return rc;
+    const size_t n4 = (size_t)M * (size_t)N / 4;
+    const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n4 + 255) / 256, (size_t)plan->sm_count * 4));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = plan->pdl ? 1 : 0;
+    const float4* w = reinterpret_cast<const float4*>(plan->d_partials);
+    cudaError_t e;
+    if (out_dtype == GEMM_F32)
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<GEMM_F32>, w, C, n4, n4, slices);
+    else if (out_dtype == GEMM_BF16)
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<GEMM_BF16>, w, C, n4, n4, slices);
+    else
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<GEMM_F16>, w, C, n4, n4, slices);
+    if (e != cudaSuccess || (ordered && cudaEventRecord(plan->split_ev, stream) != cudaSuccess)) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lr(plan->rec_mu);
+    plan->last_split = slices;
     return GEMM_OK;
 }
 
@@ -570,6 +695,11 @@ int gemm_plan_set_option(gemm_plan_t plan, int option, int64_t value) {
             plan->visible_devices = n;
             return GEMM_OK;
         }
+        case GEMM_OPT_SPLIT_K:
+            if (value != -1 && value != 0 && value != 2 && value != 4 && value != 8 && value != 16 && value != 32)
+                return GEMM_ERR_INVALID_ARG;
+            plan->split_k = (int)value;
+            return GEMM_OK;
         case GEMM_OPT_PDL:
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             plan->pdl = (int)value;
@@ -831,6 +961,13 @@ int gemm_plan_last_launch(gemm_plan_t plan, int* ctas, int* ctas_per_unit, int* 
     return GEMM_OK;
 }
 
+int gemm_plan_last_split(gemm_plan_t plan, int* slices) {
+    if (!plan || !slices) return GEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(plan->rec_mu);
+    *slices = plan->last_split;
+    return GEMM_OK;
+}
+
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n) {
     if (!plan || !tile_n) return GEMM_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(plan->rec_mu);
@@ -903,6 +1040,7 @@ int gemm_plan_destroy(gemm_plan_t plan) {
         if (plan->hbuf[i]) cudaFree(plan->hbuf[i]);
     for (int i = 0; i < 3; ++i)
         if (plan->hstream[i]) cudaStreamDestroy(plan->hstream[i]);
+    if (plan->split_ev) cudaEventDestroy(plan->split_ev);
     cudaEvent_t evs[3] = {plan->hev_start, plan->hev_b, plan->hev_done};
     for (cudaEvent_t e : evs)
         if (e) cudaEventDestroy(e);

@@ -138,4 +138,40 @@ inline bool launch_dynamic_lists(int mode, bool capped, bool stream_k, int64_t t
     return false;
 }
 
+// Split-K for problems with few tiles and a long K: the product becomes S
+// products over K slices (k-blocks [s·KB/S, (s+1)·KB/S)), one fp32 partial
+// each, then a reduction sums the S partials in order and writes C.  S is a
+// power of two up to kSplitMax that divides the k-blocks, keeps at least
+// kSplitMinKBlocks per slice, keeps every slice's tiles in one wave
+// (tiles·S <= resident units) and fits the workspace; it is the S that
+// minimises k-blocks per slice + kSplitCostKBlocks (the reduction and its
+// launch, ~3 µs ≈ 12 k-blocks of a 256-wide tile), and must beat the
+// unsplit K loop by a quarter.  `forced` > 1 asks for that S (still subject
+// to the divisibility, wave and workspace limits); 0 turns it off.
+// Returns 1 for no split.
+constexpr int kSplitMax = 32;
+constexpr int64_t kSplitMinKBlocks = 4;
+constexpr int64_t kSplitCostKBlocks = 12;
+
+inline int launch_split_k(int forced, int64_t tiles, int64_t units, int64_t k_blocks, int64_t slice_floats,
+                          int64_t workspace_floats) {
+    if (forced == 0 || tiles <= 0 || k_blocks <= 0) return 1;
+    int best = 1;
+    int64_t best_cost = k_blocks;
+    for (int s = 2; s <= kSplitMax; s *= 2) {
+        if (k_blocks % s != 0 || k_blocks / s < kSplitMinKBlocks) continue;
+        if (tiles * s > units || slice_floats * s > workspace_floats) continue;
+        if (forced > 1) {
+            if (s == forced) return s;
+            continue;
+        }
+        const int64_t cost = k_blocks / s + kSplitCostKBlocks;
+        if (cost * 4 <= k_blocks * 3 && cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 }  // namespace gb300

@@ -45,8 +45,10 @@
  * once; calls build their tensor maps on the host stack and share only
  * read-only plan state, the device status word and the last-launch record
  * (written under a lock by every run; with concurrent runs it describes one
- * of them).  Exception: with the stream-K option on (off by default) runs
- * share the plan's workspace, so runs that may overlap on the GPU must then
+ * of them).  Split products (GEMM_OPT_SPLIT_K) also share the plan's
+ * workspace; the library orders them one after another on the GPU.
+ * Exception: with the stream-K option on (off by default) runs share the
+ * plan's workspace unordered, so runs that may overlap on the GPU must then
  * use different plans.
  */
 #ifndef GB300_GEMM_H
@@ -180,6 +182,24 @@ typedef enum {
                                     last tiles' loads and MMAs are issued.  A kernel
                                     launched after it without that attribute is
                                     ordered as usual.  0: plain stream order        */
+    GEMM_OPT_SPLIT_K = 14,       /* K slices of a plain product with few tiles and a long
+                                    K: -1 (default) = chosen per problem, 0 = never, or
+                                    2, 4, 8, 16, 32 = that many where the problem allows
+                                    it.  A split product runs its K slices as a batch
+                                    of products over column slices of A and B, each
+                                    writing an fp32 partial into the plan's stream-K
+                                    workspace, then sums the partials in slice order
+                                    (deterministic) and writes C.  Only for K-major
+                                    operands, K a multiple of the k-block (64 16-bit or
+                                    128 8-bit elements) divisible into slices of at
+                                    least four k-blocks, every slice's tiles in one
+                                    wave, M·N·slices floats within the workspace, and
+                                    plans without stream-K or a CTA cap.  Split
+                                    products of one plan are ordered one after another
+                                    on the GPU, whatever their streams (an event);
+                                    inside stream capture that ordering is left to the
+                                    graph, so a plan whose split products are captured
+                                    must not run others while the graph replays     */
     GEMM_OPT_VISIBLE_DEVICES = 11 /* GPUs the plan counts as visible to the process,
                                     1..1024 (0 = default: cudaGetDeviceCount at plan
                                     creation).  TMA multicast stays within one GPU's
@@ -257,6 +277,9 @@ int gemm_plan_status(gemm_plan_t plan, int* device_status);
 
 /* Number of CTAs the last run on this plan launched (for reports). */
 int gemm_plan_last_grid(gemm_plan_t plan, int* ctas);
+
+/* K slices of the last run on this plan (1: not split; see GEMM_OPT_SPLIT_K). */
+int gemm_plan_last_split(gemm_plan_t plan, int* slices);
 
 /* Tile width BN the last run on this plan used (for reports). */
 int gemm_plan_last_tile_n(gemm_plan_t plan, int* tile_n);

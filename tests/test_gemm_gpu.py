@@ -960,6 +960,7 @@ def test_long_k(g, plan, unit):
     exact in fp32 (|sum| <= 16 K = 2^19), so the oracle's bits are the bar."""
     M, N, K = 256, 520, 32768
     configure(g, plan, unit)
+    g.gemm_plan_set_option(plan, g.GEMM_OPT_SPLIT_K, 0)   # one K loop per tile, not slices
     try:
         A, B = draw(M, N, K, dist="int", seed=101)
         C = parity.to_f64(run(g, plan, A.cuda(), B.cuda(), wl.F32))
@@ -967,6 +968,7 @@ def test_long_k(g, plan, unit):
         assert np.array_equal(C, C_ref), f"{int((C != C_ref).sum())} mismatches"
     finally:
         configure(g, plan, 4)
+        g.gemm_plan_set_option(plan, g.GEMM_OPT_SPLIT_K, -1)
 
 
 def test_k_zero_writes_zeros(g, plan):
@@ -1165,6 +1167,112 @@ def test_launch_right_after_torch_kernels_reads_their_output(g, fresh_plan):
     for bad in (-1, 2):
         assert g.raw_status("gemm_plan_set_option", ctypes.c_void_p(fresh_plan), g.GEMM_OPT_PDL,
                             ctypes.c_int64(bad)) == g.GEMM_ERR_INVALID_ARG
+
+
+# (M, N, K, input, output, split option): few tiles and a long K
+SPLIT_CASES = [(256, 256, 8192, wl.BF16, wl.F32, -1), (128, 4096, 4096, wl.F16, wl.F16, -1),
+               (384, 384, 4096, wl.BF16, wl.BF16, -1), (256, 512, 8192, wl.E4M3, wl.BF16, -1),
+               (520, 264, 4096, wl.BF16, wl.F32, 8), (1000, 776, 2048, wl.F16, wl.F32, 2)]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"_s{c[5]}")
+def test_split_k_products(g, fresh_plan, case):
+    """Products with few tiles and a long K run as K slices (fp32 partials in
+    the workspace) plus an in-order reduction: split chosen automatically or
+    forced, the result on integer inputs equal bit for bit to the unsplit
+    product and to the oracle, on random inputs within the tolerance, and
+    the same bits twice."""
+    M, N, K, dt, out, split = case
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_SPLIT_K, split)
+    A, B = draw(M, N, K, dtype=dt, dist="int", seed=M + K)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = run(g, fresh_plan, Ad, Bd, out)
+    assert g.gemm_plan_last_split(fresh_plan) > 1, "not split"
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_SPLIT_K, 0)
+    C1 = run(g, fresh_plan, Ad, Bd, out)
+    assert g.gemm_plan_last_split(fresh_plan) == 1
+    assert torch.equal(C, C1), "split and unsplit products differ on integer inputs"
+    C_ref, _ = oracle_full(A, B)
+    want = C_ref if out == wl.F32 else oracle.decode(oracle.encode(C_ref, out), out)
+    assert np.array_equal(parity.to_f64(C), want)
+    g.gemm_plan_set_option(fresh_plan, g.GEMM_OPT_SPLIT_K, split)
+    A, B = draw(M, N, K, dtype=dt, seed=M + K + 1)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = run(g, fresh_plan, Ad, Bd, out)
+    C2 = run(g, fresh_plan, Ad, Bd, out)
+    assert torch.equal(C, C2), "split product not repeatable"
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(parity.to_f64(C), C_ref, S, out, f"split {case}")
+
+
+def test_split_k_rules(g, fresh_plan):
+    """No split where it cannot pay or is not allowed: many tiles, short K,
+    K not a whole number of k-blocks, MN-major operands, option 0."""
+    import ctypes
+    for M, N, K in ((4096, 4096, 4096), (256, 256, 256), (256, 256, 8200)):
+        A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+        B = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+        run(g, fresh_plan, A, B, wl.F32)
+        assert g.gemm_plan_last_split(fresh_plan) == 1, (M, N, K)
+    A, B = draw(256, 256, 8192, seed=5)
+    C = run_layout(g, fresh_plan, A.cuda(), B.cuda(), 2, wl.F32)
+    assert g.gemm_plan_last_split(fresh_plan) == 1
+    C_ref, S = oracle_full(A, B)
+    parity.assert_within(parity.to_f64(C), C_ref, S, wl.F32, "MN-major B, not split")
+    for bad in (1, 3, 64, -2):
+        assert g.raw_status("gemm_plan_set_option", ctypes.c_void_p(fresh_plan), g.GEMM_OPT_SPLIT_K,
+                            ctypes.c_int64(bad)) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_split_k_from_two_streams_on_one_plan(g, fresh_plan):
+    """Split products share the plan's workspace: issued from two streams at
+    once they are ordered on the GPU by the library, so every result is
+    exact."""
+    M, N, K = 256, 256, 8192
+    data = [draw(M, N, K, dist="int", seed=300 + i) for i in range(2)]
+    refs = [oracle_full(A, B)[0] for A, B in data]
+    dev = [(A.cuda(), B.cuda()) for A, B in data]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    for _ in range(20):
+        for i in range(2):
+            C = torch.full((M, N), float("nan"), device="cuda")
+            g.gemm_plan_run(fresh_plan, dev[i][0].data_ptr(), dev[i][1].data_ptr(), C.data_ptr(), M, N, K, wl.BF16,
+                            wl.F32, streams[i].cuda_stream)
+            outs[i].append(C)
+    torch.cuda.synchronize()
+    assert g.gemm_plan_status(fresh_plan) == 0
+    assert g.gemm_plan_last_split(fresh_plan) > 1
+    for i in range(2):
+        for C in outs[i]:
+            assert np.array_equal(parity.to_f64(C), refs[i]), f"stream {i}"
+
+
+def test_split_k_in_cuda_graph(g, fresh_plan):
+    """A split product (slices and reduction) recorded into a CUDA graph and
+    replayed on new integer inputs equals the oracle every time."""
+    M, N, K = 384, 384, 4096
+    Ad = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    Bd = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    Cd = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                        s.cuda_stream)
+    s.synchronize()
+    assert g.gemm_plan_last_split(fresh_plan) > 1
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.gemm_plan_run(fresh_plan, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, wl.BF16, wl.F32,
+                        s.cuda_stream)
+    for rep in range(3):
+        A, B = draw(M, N, K, dist="int", seed=70 + rep)
+        Ad.copy_(A)
+        Bd.copy_(B)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(parity.to_f64(Cd), oracle_full(A, B)[0]), rep
+    assert g.gemm_plan_status(fresh_plan) == 0
 
 
 def test_clock_log_records_each_launch(g, fresh_plan):

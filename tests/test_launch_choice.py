@@ -134,3 +134,33 @@ def test_single_ctas_for_small_problems(choose):
     assert choose(256, 256, 256, pair=2)["unit"] == 2
     assert choose(1000, 776, 1256, mc=1)["unit"] == 4
     assert choose(4096, 4096, 4096, pair=1)["unit"] == 1
+
+
+@pytest.fixture(scope="module")
+def split(tmp_path_factory):
+    exe = str(tmp_path_factory.mktemp("split") / "split_dump")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, "-I", INCLUDE,
+                    os.path.join(ROOT, "tests", "native", "split_dump.cpp"), "-o", exe], check=True)
+
+    def run(tiles, units, kb, slice_floats, forced=-1, ws=152 * 4 * 8192):
+        line = f"{forced} {tiles} {units} {kb} {slice_floats} {ws}\n"
+        return int(subprocess.run([exe], input=line, capture_output=True, text=True, check=True).stdout)
+    return run
+
+
+def test_split_k_choice(split):
+    """K slices: a power of two dividing the k-blocks, at least four k-blocks
+    each, every slice's tiles in one wave, the partials within the
+    workspace; the count minimising k-blocks per slice + a fixed reduction
+    cost, and only where that beats the unsplit K loop by a quarter."""
+    assert split(4, 152, 128, 256 * 256) == 32          # 256×256×8192 on single CTAs: 4 k-blocks per slice
+    assert split(32, 152, 64, 128 * 4096) == 4          # 128×4096×4096: 32 tiles, 4 slices fill the wave
+    assert split(9, 152, 64, 384 * 384) == 16           # 384×384×4096
+    assert split(76, 76, 64, 1024 * 4096) == 1          # a full wave of tiles already
+    assert split(4, 152, 4, 256 * 256) == 1             # 256³: four k-blocks in all
+    assert split(64, 152, 16, 1024 * 1024) == 1         # 1024³: a split saves too little
+    assert split(4, 152, 128, 4096 * 4096) == 1         # the partials would not fit the workspace
+    assert split(4, 152, 100, 65536) == 4               # 100 k-blocks: 4 divides, 8 does not
+    assert split(4, 152, 128, 65536, forced=0) == 1     # off
+    assert split(4, 152, 128, 65536, forced=8) == 8     # asked for
+    assert split(40, 152, 128, 65536, forced=8) == 1    # 320 slices' tiles would not fit one wave
