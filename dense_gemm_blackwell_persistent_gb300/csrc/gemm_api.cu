@@ -369,8 +369,7 @@ int launch(gemm_plan* plan, const void* A, const void* B, void* C, int64_t M, in
     p.num_tiles = (int)(p.tiles_per_batch * batch.count);
     p.a_batched = batch.count > 1 && batch.sa != 0;
     p.b_batched = batch.count > 1 && batch.sb != 0;
-    p.group_m = plan->group_m > 0 ? plan->group_m : 8;
-    p.group_m = std::max(1, std::min(p.group_m, p.tiles_m));
+    p.group_m = launch_group_m(plan->group_m, p.tiles_m, M * K * elem_bytes(dtype));
     p.fd_batch = make_fastdiv((uint32_t)p.tiles_per_batch);
     p.fd_group = make_fastdiv((uint32_t)(p.group_m * p.tiles_n));
     p.fd_gm = make_fastdiv((uint32_t)p.group_m);

@@ -23,6 +23,20 @@ constexpr int kLaunchWidths[kLaunchTileWidths] = {256, 224, 192, 160, 128};   //
 constexpr int kLaunchRowsPerCta = 128;   // rows of A per CTA (TMEM lanes)
 constexpr int kLaunchMnBox = 64;         // elements of M or N per MN-major TMA box
 
+// Raster group height (tile rows walked column by column together) when the
+// caller leaves it to the library: all the tile rows when one batch
+// element's A is at most kWholeGroupABytes, so that the waves walk the
+// columns once with A resident in L2; else 8.  Measured on GB300: 4096³
+// (A 32 MB) sustained for 4 s +1.0–1.5% with the whole height (16) over 8
+// in three runs, bursts level; 8192³ (A 128 MB) level from 8 to 16.
+constexpr int64_t kWholeGroupABytes = int64_t(48) << 20;
+
+inline int launch_group_m(int forced, int64_t tiles_m, int64_t a_bytes) {
+    int g = forced > 0 ? forced : (a_bytes <= kWholeGroupABytes ? (int)(tiles_m < (1 << 20) ? tiles_m : 1 << 20) : 8);
+    if (g > tiles_m) g = (int)tiles_m;
+    return g < 1 ? 1 : g;
+}
+
 // CTAs per MMA when the caller leaves it to the library (option 0): single
 // CTAs for problems too small to fill half a wave of CTA pairs, as long as
 // their 128×128 tiles still fit in one wave of single CTAs; pairs

@@ -112,7 +112,8 @@ typedef enum {
                                     problems under half a wave of pair tiles that fit
                                     one wave of 128×128 single-CTA tiles (there a
                                     pair's set-up costs more than it saves)         */
-    GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto) */
+    GEMM_OPT_GROUP_M = 2,        /* rasterisation group height in tiles, >= 1 (0 = auto:
+                                    every tile row when A is at most 48 MB, else 8)  */
     GEMM_OPT_MAX_CTAS = 3,       /* cap on resident CTAs of the persistent grid (0 = all SMs) */
     GEMM_OPT_TILE_N = 4,         /* tile width: 256, 224, 192, 160 or 128 (0 = default:
                                     chosen per problem to fill whole waves)             */

@@ -164,3 +164,27 @@ def test_split_k_choice(split):
     assert split(4, 152, 128, 65536, forced=0) == 1     # off
     assert split(4, 152, 128, 65536, forced=8) == 8     # asked for
     assert split(40, 152, 128, 65536, forced=8) == 1    # 320 slices' tiles would not fit one wave
+
+
+def test_group_height_rule(tmp_path):
+    """Raster group height left to the library: every tile row when A is at
+    most 48 MB (4096³ bf16: 32 MB, 16 rows of pairs), else 8; never more
+    than the tile rows; a forced height is kept (clipped to the tile rows)."""
+    src = tmp_path / "group_dump.cpp"
+    src.write_text('#include <cstdio>\n#include "launch_choice.h"\nint main(){long long f,t,a;'
+                   'while(std::scanf("%lld %lld %lld",&f,&t,&a)==3)std::printf("%d\\n",'
+                   'gb300::launch_group_m((int)f,t,a));}\n')
+    exe = str(tmp_path / "group_dump")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-I", CSRC, "-I", INCLUDE, str(src), "-o", exe], check=True)
+
+    def group(forced, tiles_m, a_bytes):
+        out = subprocess.run([exe], input=f"{forced} {tiles_m} {a_bytes}\n", capture_output=True, text=True,
+                             check=True).stdout
+        return int(out)
+    assert group(0, 16, 4096 * 4096 * 2) == 16       # bf16 4096³
+    assert group(0, 32, 8192 * 8192 * 2) == 8        # bf16 8192³
+    assert group(0, 4, 1024 * 4096 * 2) == 4         # the one-wave shape: its 4 rows
+    assert group(0, 8, 4000 * 5000 * 2) == 8         # ragged, 4-CTA units: 40 MB, all 8 rows
+    assert group(0, 3, 10 ** 9) == 3                 # never more than the tile rows
+    assert group(4, 16, 4096 * 4096 * 2) == 4        # forced
+    assert group(64, 16, 10 ** 9) == 16
