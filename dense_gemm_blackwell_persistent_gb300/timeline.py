@@ -26,8 +26,8 @@ from . import (GEMM_OPT_CTA_PAIR, GEMM_OPT_DYNAMIC, GEMM_OPT_MAX_CTAS, GEMM_OPT_
                gemm_plan_create, gemm_plan_destroy, gemm_plan_last_grid, gemm_plan_last_launch, gemm_plan_run,
                gemm_plan_set_option, gemm_plan_trace)
 
-POINTS = {0: "entry", 3: "first_full", 11: "epilogue_stores_done", 4: "teardown", 12: "cluster_arrived",
-          13: "cluster_done", 14: "tmem_dealloc", 5: "exit"}
+POINTS = {0: "entry", 3: "first_full", 86: "epilogue_loop_done", 11: "epilogue_stores_done", 84: "producer_done",
+          85: "mma_warp_done", 4: "teardown", 12: "cluster_arrived", 13: "cluster_done", 14: "tmem_dealloc", 5: "exit"}
 ITEMS = {16: "mma_end", 24: "epi_start", 32: "epi_end", 40: "partial_published", 48: "reduce_done"}
 TOTALS = {6: "mma_wait_full_us", 7: "producer_wait_empty_us", 8: "mma_wait_acc_empty_us",
           1: "producer_wait_response_us", 10: "mma_wait_response_us", 2: "epilogue_wait_response_us"}
