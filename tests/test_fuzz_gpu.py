@@ -23,7 +23,7 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-CASES = 96
+CASES = 400
 
 
 def make_case(i: int) -> dict:
