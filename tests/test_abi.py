@@ -131,3 +131,24 @@ def test_torch_helpers_refuse_host_tensors(lib):
         lib.matmul(A, B.t().contiguous(), b_kn=True)
     with pytest.raises(ValueError, match="CUDA tensors"):
         lib.bmm(A.view(1, 64, 64), B)
+
+
+def build_c_caller(lib_path, exe):
+    """Compile tests/native/c_caller.c as strict C99 against include/gemm.h and
+    link it to the library (rpath to the library's folder)."""
+    import subprocess
+    src = os.path.join(ROOT, "tests", "native", "c_caller.c")
+    lib_dir = os.path.dirname(lib_path)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-O1", "-I", os.path.join(ROOT, "include"),
+           src, "-o", exe, "-L", lib_dir, "-l:" + os.path.basename(lib_path), "-Wl,-rpath," + lib_dir]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+
+
+def test_plain_c_caller_compiles_and_links(lib, tmp_path):
+    """The header is valid C99 without CUDA headers, and a C program that
+    calls the boundary links against the library (run on a GPU by the GPU
+    tests; here only with --link-only, which exits before any call)."""
+    import subprocess
+    exe = str(tmp_path / "c_caller")
+    build_c_caller(lib.LIB_PATH, exe)
+    assert subprocess.run([exe, "--link-only"]).returncode == 0

@@ -1518,3 +1518,17 @@ def test_torch_matmul_helper(g, plan):
     torch.cuda.synchronize()
     C_ref, S = oracle_full(A, B)
     parity.assert_within(parity.to_f64(C), C_ref, S, wl.F32, "matmul helper")
+
+
+def test_plain_c_caller_bit_exact(g, tmp_path):
+    """A C99 program with no CUDA headers (tests/native/c_caller.c) runs a
+    ragged integer product through gemm_plan_run_host and checks every
+    element against an exact integer loop, then checks that bad arguments
+    come back as codes."""
+    import subprocess
+    from tests.test_abi import build_c_caller
+    exe = str(tmp_path / "c_caller")
+    build_c_caller(g.LIB_PATH, exe)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c caller ok" in r.stdout
